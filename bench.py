@@ -1,0 +1,419 @@
+"""Benchmark: BF16 x NVFP4 GEMM on the Llama-3-70B linear shapes.
+
+One step = one pass of the hot path over one batch: the four linear layers of
+a Llama-3-70B block (QKV 10240x8192, O 8192x8192, gate_up 57344x8192,
+down 8192x28672; W stored [n, k]) at decode size m = 16, NVFP4 weights with
+16-element E4M3 scales and global scale 1, A ~ N(0,1), W ~ N(0,0.02)
+(synthetic, seeded).  Weights are quantised and repacked offline (before the
+timed region).  Two weight copies (2 x 481 MB, far above the 129 MB L2) are
+used on alternate steps, so every weight byte comes from HBM.
+
+value = algorithmic bytes (packed weights + scales + A + C) of all steps on
+all ranks / max-over-ranks time, in GB/s.  Each GEMM is replayed as a CUDA
+graph; CUDA events between them give every kernel's duration.
+
+--impl reference times the FP64 CPU oracle (dequantise + GEMM) on a bounded
+sample of the same workload instead.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BF16×NVFP4 GEMM TFLOP/s & HBM GB/s (% roofline), Llama-3-70B shapes m=16/256"
+SHAPES = [("qkv", 10240, 8192), ("o", 8192, 8192), ("gate_up", 57344, 8192), ("down", 8192, 28672)]
+M_DECODE = 16
+M_PREFILL = 256
+PAGE = 4096
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algo_bytes(m, n, k, scale_group=16):
+    """Packed FP4 weights + block scales + A + C bytes of one GEMM."""
+    return n * k // 2 + n * k // scale_group + 2 * m * k + 2 * m * n
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def ncu_traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", kernel_file)
+    src = os.path.join(ROOT, "fp4_weight_only_gb300", "csrc", "gemm.cu")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("-"):
+                key, val = line.strip()[1:].split(":", 1)
+                fields[key.strip()] = val.strip()
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("gemm.cu sha256[:16]") != digest:
+        return None
+    try:
+        return float(fields["dram bytes per launch (gate_up, scaled)"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples (200 ms period)."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu=timestamp,{self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        import datetime
+        rows = []
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------------- oracle
+def oracle_sample(weights_cpu, acts_cpu, rows):
+    """Time the FP64 oracle (dequant + GEMM) on the first `rows` rows of each
+    weight matrix; quantisation is done first and not timed."""
+    from oracle import gemm as og
+    from oracle import quantize as oq
+    prepared = []
+    for (name, n, k), w, a in zip(SHAPES, weights_cpu, acts_cpu):
+        codes, scales = oq.nvfp4_quantize(w[:rows].float().numpy(), 1.0)
+        prepared.append((a.float().numpy(), codes, scales, k))
+    t0 = time.perf_counter()
+    for a, codes, scales, k in prepared:
+        og.gemm(a, og.dequantize(codes, scales, "nvfp4"), 1.0)
+    dt = time.perf_counter() - t0
+    nbytes = sum(algo_bytes(M_DECODE, rows, k) for _, _, _, k in prepared)
+    return nbytes, dt
+
+
+def synth_inputs_cpu(rows):
+    from fp4_weight_only_gb300 import synth
+    ws = [synth.weights(rows, k, seed=100 + i) for i, (_, n, k) in enumerate(SHAPES)]
+    acts = [synth.activations(M_DECODE, k, seed=200 + i) for i, (_, n, k) in enumerate(SHAPES)]
+    return ws, acts
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rows = 96
+    ws, acts = synth_inputs_cpu(rows)
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample(ws, acts, rows)
+    total_b, total_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = oracle_sample(ws, acts, rows)
+        total_b += b
+        total_t += t
+    value = total_b / total_t / 1e9
+    sample = (f"{rows} seeded N(0,0.02) rows for each of the 4 Llama-3-70B weight shapes, m={M_DECODE}; "
+              "oracle NVFP4 dequantise + FP64 GEMM per step (quantisation untimed)")
+    cores = os.cpu_count()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "llama3-70b linears, NVFP4 decode m=16 (sample)",
+                                        "m": M_DECODE, "rows_per_matrix": rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------------ GPU
+def run_ours(args, rank, world, local):
+    from fp4_weight_only_gb300 import binding, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)        # graphs are captured and replayed off the default stream
+    torch.cuda.set_stream(stream)
+
+    # offline preparation: quantise + repack on the GPU (not timed)
+    sets = [[], []]
+    acts, outs = [], []
+    for i, (name, n, k) in enumerate(SHAPES):
+        w = synth.weights(n, k, seed=100 + i, device=dev)
+        fw = binding.FP4Weight(w, "nvfp4", 1.0)
+        del w
+        sets[0].append(fw)
+        sets[1].append((fw.w_rep.clone(), fw.s_rep.clone()))
+        acts.append(synth.activations(M_DECODE, k, seed=200 + i, device=dev))
+        outs.append(torch.empty((M_DECODE, n), dtype=torch.bfloat16, device=dev))
+    ws = binding.Workspace(dev)
+    for (name, n, k) in SHAPES:
+        ws.ensure(binding.workspace_bytes(M_PREFILL, n, k))
+    torch.cuda.synchronize()
+
+    def launch(i, which, m=M_DECODE, a=None, c=None):
+        fw = sets[0][i]
+        wr, sr = (fw.w_rep, fw.s_rep) if which == 0 else sets[1][i]
+        binding.gemm(acts[i] if a is None else a, wr, sr, fw.n, "nvfp4", 1.0, workspace=ws,
+                     out=outs[i] if c is None else c)
+
+    # one CUDA graph per (GEMM, weight copy)
+    for i in range(len(SHAPES)):
+        for which in (0, 1):
+            launch(i, which)
+    torch.cuda.synchronize()
+    graphs = {}
+    for i in range(len(SHAPES)):
+        for which in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                launch(i, which)
+            graphs[(i, which)] = g
+    torch.cuda.synchronize()
+
+    def step(s, evs=None):
+        for i in range(len(SHAPES)):
+            if evs is not None:
+                evs[i].record(stream)
+            graphs[(i, s & 1)].replay()
+        if evs is not None:
+            evs[len(SHAPES)].record(stream)
+
+    sampler = ClockSampler(local)
+    for s in range(args.warmup):
+        step(s)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(SHAPES) + 1)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    start.record(stream)
+    for s in range(args.steps):
+        step(s, evs[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_host1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    elapsed_ms = start.elapsed_time(end)
+    per_kernel_ms = np.zeros(len(SHAPES))
+    for s in range(args.steps):
+        for i in range(len(SHAPES)):
+            per_kernel_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    per_kernel_ms /= args.steps
+    elapsed_max = elapsed_ms
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_max = float(t.item())
+
+    step_bytes = sum(algo_bytes(M_DECODE, n, k) for _, n, k in SHAPES)
+    step_flops = sum(2 * M_DECODE * n * k for _, n, k in SHAPES)
+    ms_per_step = elapsed_max / args.steps
+    value = world * step_bytes * args.steps / (elapsed_max * 1e-3) / 1e9
+    shapes = {}
+    for i, (name, n, k) in enumerate(SHAPES):
+        t = per_kernel_ms[i] * 1e-3
+        b = algo_bytes(M_DECODE, n, k)
+        shapes[name] = {"n": n, "k": k, "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1),
+                        "tflops": round(2 * M_DECODE * n * k / t / 1e12, 2),
+                        "weight_gbs": round((n * k // 2 + n * k // 16) / t / 1e9, 1),
+                        "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3)}
+    kernel_bytes = step_bytes
+    kernel_time = float(per_kernel_ms.sum()) * 1e-3
+    achieved = kernel_bytes / kernel_time / 1e9
+    traffic = ncu_traffic("gemm_nvfp4_decode_m16.txt")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": "gemm_kernel<NVFP4, BN=16> (all four launches of a step)",
+                "peak_source": peaks["source"] + " hbm_gbs (copy bandwidth)"}
+
+    # e2e: public API per step with pinned host activations in and results out
+    a_host = [a.cpu().pin_memory() for a in acts]
+    c_host = [torch.empty((M_DECODE, n), dtype=torch.bfloat16).pin_memory() for _, n, _ in SHAPES]
+    a_dev = [torch.empty_like(a) for a in acts]
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step(s):
+        for i, (name, n, k) in enumerate(SHAPES):
+            a_dev[i].copy_(a_host[i], non_blocking=True)
+            fw = sets[0][i]
+            wr, sr = (fw.w_rep, fw.s_rep) if (s & 1) == 0 else sets[1][i]
+            c = binding.gemm(a_dev[i], wr, sr, n, "nvfp4", 1.0, workspace=ws)
+            c_host[i].copy_(c, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for s in range(3):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        e2e_step(s)
+    e2e_t = time.perf_counter() - t0
+    h2d = sum(2 * M_DECODE * k for _, _, k in SHAPES)
+    d2h = sum(2 * M_DECODE * n for _, n, _ in SHAPES)
+    e2e = {"value": round(world * step_bytes * e2e_steps / e2e_t / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "path": "binding.gemm (ctypes -> C ABI) per layer, eager, pinned host buffers"}
+
+    # prefill m = 256 (same kernels, tcgen05 N = 128 tiles), per-GEMM timing
+    prefill = None
+    if not args.no_prefill:
+        pa = [synth.activations(M_PREFILL, k, seed=300 + i, device=dev, outlier_frac=0.001)
+              for i, (_, n, k) in enumerate(SHAPES)]
+        pc = [torch.empty((M_PREFILL, n), dtype=torch.bfloat16, device=dev) for _, n, _ in SHAPES]
+        pg = {}
+        for i in range(len(SHAPES)):
+            for which in (0, 1):
+                launch(i, which, M_PREFILL, pa[i], pc[i])
+        torch.cuda.synchronize()
+        for i in range(len(SHAPES)):
+            for which in (0, 1):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    launch(i, which, M_PREFILL, pa[i], pc[i])
+                pg[(i, which)] = g
+        reps = 50
+        prefill = {}
+        for i, (name, n, k) in enumerate(SHAPES):
+            for r in range(5):
+                pg[(i, r & 1)].replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(reps):
+                pg[(i, r & 1)].replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / reps * 1e-3
+            tf = 2 * M_PREFILL * n * k / t / 1e12
+            prefill[name] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
+                             "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = 512
+        w_cpu = [synth.weights(n, k, seed=100 + i, device=dev)[:rows].cpu() for i, (_, n, k) in enumerate(SHAPES)]
+        a_cpu = [a.cpu() for a in acts]
+        nb, dt = oracle_sample(w_cpu, a_cpu, rows)
+        cpu_baseline = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                        "kind": "oracle",
+                        "sample": f"first {rows} rows of each of the 4 weight matrices (same seeded weights), "
+                                  f"m={M_DECODE}; NVFP4 dequantise + FP64 GEMM with numpy, quantisation untimed; "
+                                  f"{dt:.1f} s"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights quantised to NVFP4 on the GPU)",
+            "config": {"workload": "llama3-70b linears qkv/o/gate_up/down, NVFP4 decode m=16, g=1",
+                       "m": M_DECODE, "shapes_nk": [[n, k] for _, n, k in SHAPES],
+                       "l2": "2 rotating weight sets of 481 MB each (> 129 MB L2)",
+                       "parallelism": f"replicas x{world}"},
+            "tflops": round(world * step_flops * args.steps / (elapsed_max * 1e-3) / 1e12, 2),
+            "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+            "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks, "prefill_m256": prefill,
+        }
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1 and args.impl != "reference":
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+"""Thin ctypes binding of the C ABI in include/petit.h.
+
+Argument marshalling only: every computation runs in the CUDA library.  The
+functions take torch tensors for device memory and use torch's current CUDA
+stream.  If the library cannot be built or loaded, :func:`load` raises --
+there is no CPU fallback.
+"""
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PETIT_FMT_NVFP4 = 0
+PETIT_FMT_MXFP4 = 1
+FORMATS = {"nvfp4": PETIT_FMT_NVFP4, "mxfp4": PETIT_FMT_MXFP4}
+
+STATUS = {
+    0: "PETIT_OK",
+    1: "PETIT_ERR_INVALID_ARG",
+    2: "PETIT_ERR_UNSUPPORTED_SHAPE",
+    3: "PETIT_ERR_MISALIGNED",
+    4: "PETIT_ERR_WORKSPACE",
+    5: "PETIT_ERR_ARCH",
+    6: "PETIT_ERR_CUDA",
+    7: "PETIT_ERR_TIMEOUT",
+}
+
+_lib = None
+_lock = threading.Lock()
+
+_c_i64 = ctypes.c_int64
+_c_p = ctypes.c_void_p
+_c_sz = ctypes.c_size_t
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "petit_layout_version": (ctypes.c_int, []),
+    "petit_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "petit_repacked_weight_bytes": (_c_sz, [_c_i64, _c_i64]),
+    "petit_repacked_scale_bytes": (_c_sz, [_c_i64, _c_i64, ctypes.c_int]),
+    "petit_gemm_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "petit_absmax_bf16": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p]),
+    "petit_nvfp4_global_scale": (ctypes.c_float, [ctypes.c_float]),
+    "petit_quantize_nvfp4": (ctypes.c_int, [_c_p, ctypes.c_float, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_quantize_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_repack_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_repack_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_dequant_bf16": (ctypes.c_int, [_c_p, _c_p, ctypes.c_int, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64,
+                                             _c_i64, _c_p, _c_sz, _c_p]),
+    "petit_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p,
+                                             _c_sz, _c_p]),
+    "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
+    "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
+}
+
+
+class PetitError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def load(build=True):
+    """Build (if stale) and load the CUDA library; raises on failure."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def lib_path():
+    return _build.LIB
+
+
+def _check(status, where):
+    if status != 0:
+        raise PetitError(status, where)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: need a contiguous CUDA {dtype} tensor")
+
+
+# ---------------------------------------------------------------------- API
+def layout_version():
+    return load().petit_layout_version()
+
+
+def absmax(x):
+    """max |x| of a BF16 CUDA tensor, as a 1-element FP32 CUDA tensor."""
+    _need(x, torch.bfloat16, "x")
+    out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(load().petit_absmax_bf16(_ptr(x), x.numel(), _ptr(out), _stream()), "absmax")
+    return out
+
+
+def nvfp4_global_scale(amax):
+    return float(load().petit_nvfp4_global_scale(ctypes.c_float(float(amax))))
+
+
+def quantize(W, fmt="nvfp4", global_scale=1.0):
+    """BF16 [n, k] -> (packed codes uint8 [n, k/2], scales uint8 [n, k/G])."""
+    _need(W, torch.bfloat16, "W")
+    n, k = W.shape
+    group = 16 if fmt == "nvfp4" else 32
+    wp = torch.empty((n, k // 2), dtype=torch.uint8, device=W.device)
+    sp = torch.empty((n, max(k // group, 1)), dtype=torch.uint8, device=W.device)
+    L = load()
+    if fmt == "nvfp4":
+        st = L.petit_quantize_nvfp4(_ptr(W), ctypes.c_float(global_scale), _ptr(wp), _ptr(sp), n, k, _stream())
+    else:
+        st = L.petit_quantize_mxfp4(_ptr(W), _ptr(wp), _ptr(sp), n, k, _stream())
+    _check(st, "quantize_" + fmt)
+    return wp, sp
+
+
+def repack(w_packed, scales, fmt="nvfp4"):
+    """Packed codes [n, k/2] + scales -> repacked (weights, scales) uint8."""
+    _need(w_packed, torch.uint8, "w_packed")
+    _need(scales, torch.uint8, "scales")
+    n, half_k = w_packed.shape
+    k = half_k * 2
+    L = load()
+    wo = torch.empty(L.petit_repacked_weight_bytes(n, k), dtype=torch.uint8, device=w_packed.device)
+    so = torch.empty(max(L.petit_repacked_scale_bytes(n, k, FORMATS[fmt]), 1), dtype=torch.uint8,
+                     device=w_packed.device)
+    fn = L.petit_repack_nvfp4 if fmt == "nvfp4" else L.petit_repack_mxfp4
+    _check(fn(_ptr(w_packed), _ptr(scales), _ptr(wo), _ptr(so), n, k, _stream()), "repack_" + fmt)
+    return wo, so
+
+
+def dequant(w_rep, s_rep, n, k, fmt="nvfp4"):
+    """Repacked weights -> BF16 Wq [n, k] (test hook; bit-exact)."""
+    out = torch.empty((n, k), dtype=torch.bfloat16, device=w_rep.device)
+    _check(load().petit_dequant_bf16(_ptr(w_rep), _ptr(s_rep), FORMATS[fmt], _ptr(out), n, k, _stream()),
+           "dequant")
+    return out
+
+
+def workspace_bytes(m, n, k, fmt="nvfp4"):
+    return int(load().petit_gemm_workspace_bytes(m, n, k, FORMATS[fmt]))
+
+
+class Workspace:
+    """A zero-filled device workspace that grows on demand."""
+
+    def __init__(self, device=None, nbytes=0):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes):
+        if nbytes > self.buf.numel():
+            self.buf = torch.zeros(int(nbytes), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    def status(self):
+        """PETIT_OK (0) or the error the kernels recorded (clears it)."""
+        return load().petit_get_device_status(_ptr(self.buf), _stream())
+
+
+def gemm(A, w_rep, s_rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
+    """C[m, n] = g * A @ dequant(W)^T in BF16 (FP32 accumulation)."""
+    _need(A, torch.bfloat16, "A")
+    m, k = A.shape
+    ws = workspace or Workspace(A.device)
+    need = workspace_bytes(m, n, k, fmt)
+    if need == 0:
+        raise PetitError(2, "gemm workspace size")
+    buf = ws.ensure(need)
+    C = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=A.device)
+    L = load()
+    if fmt == "nvfp4":
+        st = L.petit_gemm_bf16_nvfp4(_ptr(A), _ptr(w_rep), _ptr(s_rep), ctypes.c_float(global_scale), _ptr(C),
+                                     m, n, k, _ptr(buf), buf.numel(), _stream())
+    else:
+        st = L.petit_gemm_bf16_mxfp4(_ptr(A), _ptr(w_rep), _ptr(s_rep), _ptr(C), m, n, k, _ptr(buf),
+                                     buf.numel(), _stream())
+    _check(st, "gemm_" + fmt)
+    return C
+
+
+def selftest_timeout(workspace, timeout_us=1000):
+    _check(load().petit_selftest_timeout(_ptr(workspace.buf), workspace.buf.numel(), timeout_us, _stream()),
+           "selftest_timeout")
+
+
+class FP4Weight:
+    """Offline-prepared FP4 weight: quantised, repacked, ready for gemm()."""
+
+    def __init__(self, W, fmt="nvfp4", global_scale=None):
+        n, k = W.shape
+        self.n, self.k, self.fmt = n, k, fmt
+        if fmt == "nvfp4":
+            if global_scale is None:
+                global_scale = 1.0
+            elif global_scale == "amax":
+                global_scale = nvfp4_global_scale(absmax(W).item())
+            self.global_scale = float(global_scale)
+        else:
+            self.global_scale = 1.0
+        self.w_packed, self.scales = quantize(W, fmt, self.global_scale)
+        self.w_rep, self.s_rep = repack(self.w_packed, self.scales, fmt)
+
+    def __call__(self, A, workspace=None, out=None):
+        return gemm(A, self.w_rep, self.s_rep, self.n, self.fmt, self.global_scale, workspace, out)

@@ -1,0 +1,266 @@
+// C ABI: argument validation, problem planning, tensor-map encoding and
+// kernel dispatch.  Validation always comes first and never touches the GPU,
+// so a rejected call enqueues nothing.
+#include <cstring>
+#include <mutex>
+
+#include "../../include/petit.h"
+#include "fp4_layout.cuh"
+#include "internal.h"
+
+namespace {
+
+using petit::kMXFP4;
+using petit::kNVFP4;
+
+constexpr int64_t kMaxDim = int64_t(1) << 24;
+constexpr uint64_t kGemmTimeoutNs = 2000000000ull;  // no legitimate wait lasts 2 s
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+  bool probed = false;
+  bool arch_ok = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+// Current device, its SM count, and whether it is a compute-capability 10.3
+// part (the only code this library contains is sm_103a).
+petit_status_t current_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return PETIT_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PETIT_ERR_CUDA;
+    }
+    d.arch_ok = (major == 10 && minor == 3);
+    d.num_sms = n;
+    d.probed = true;
+  }
+  if (sms) *sms = d.num_sms;
+  return d.arch_ok ? PETIT_OK : PETIT_ERR_ARCH;
+}
+
+petit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? PETIT_OK : PETIT_ERR_CUDA; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// A [m][k] BF16, boxes of 64 k x bn rows, 128-byte swizzle, zero fill outside.
+petit_status_t encode_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t k, int bn) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PETIT_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bn)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PETIT_OK : PETIT_ERR_CUDA;
+}
+
+petit_status_t check_tiled_shape(int64_t n, int64_t k) {
+  if (n < petit::kTileN || k < petit::kStageK || n % petit::kTileN || k % petit::kStageK ||
+      n > kMaxDim || k > kMaxDim)
+    return PETIT_ERR_UNSUPPORTED_SHAPE;
+  return PETIT_OK;
+}
+
+petit_status_t gemm_common(int fmt, const void* A, const uint8_t* w, const uint8_t* s,
+                           float alpha, void* C, int64_t m, int64_t n, int64_t k, void* ws,
+                           size_t ws_bytes, petit_stream_t stream) {
+  if (!A || !w || !s || !C || m < 1) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(w) || !aligned16(s) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
+  if (!ws) return PETIT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
+  int sms = 0;
+  if (petit_status_t st = current_device(&sms)) return st;
+  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, fmt, sms);
+  if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn)) return st;
+  petit::GemmArgs args{A, w, s, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int petit_layout_version(void) { return petit::kLayoutVersion; }
+
+const char* petit_status_string(petit_status_t s) {
+  switch (s) {
+    case PETIT_OK: return "ok";
+    case PETIT_ERR_INVALID_ARG: return "invalid argument";
+    case PETIT_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case PETIT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case PETIT_ERR_WORKSPACE: return "workspace missing or too small";
+    case PETIT_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case PETIT_ERR_CUDA: return "CUDA runtime error";
+    case PETIT_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t petit_repacked_weight_bytes(int64_t n, int64_t k) {
+  if (n < 0 || k < 0) return 0;
+  return static_cast<size_t>(n) * static_cast<size_t>(k) / 2;
+}
+
+size_t petit_repacked_scale_bytes(int64_t n, int64_t k, int fmt) {
+  if (n < 0 || k < 0) return 0;
+  if (fmt == PETIT_FMT_NVFP4) return static_cast<size_t>(n) * static_cast<size_t>(k) / 16;
+  if (fmt == PETIT_FMT_MXFP4) return static_cast<size_t>(n) * static_cast<size_t>(k) / 32;
+  return 0;
+}
+
+size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt) {
+  if (m < 1 || m > kMaxDim || check_tiled_shape(n, k) != PETIT_OK) return 0;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return 0;
+  int sms = 0;
+  if (current_device(&sms) != PETIT_OK) return 0;
+  return petit::plan_gemm(m, n, k, fmt, sms).ws.total;
+}
+
+petit_status_t petit_absmax_bf16(const void* x, int64_t count, float* amax_out,
+                                 petit_stream_t stream) {
+  if (!x || !amax_out || count < 1) return PETIT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(amax_out) & 3u))
+    return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(petit::launch_absmax(x, count, amax_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+float petit_nvfp4_global_scale(float amax) { return amax / (6.0f * 448.0f); }
+
+static petit_status_t quantize_common(int fmt, const void* W, float g, uint8_t* wp, uint8_t* sp,
+                                      int64_t n, int64_t k, petit_stream_t stream) {
+  if (!W || !wp || !sp || n < 1 || k < 1) return PETIT_ERR_INVALID_ARG;
+  const int64_t blk = fmt == PETIT_FMT_NVFP4 ? 16 : 32;
+  if (k % blk || n > kMaxDim || k > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(W) || !aligned16(wp) || !aligned16(sp)) return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(
+      petit::launch_quantize(fmt, W, g, wp, sp, n, k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+petit_status_t petit_quantize_nvfp4(const void* W, float global_scale, uint8_t* w_packed,
+                                    uint8_t* s_e4m3, int64_t n, int64_t k,
+                                    petit_stream_t stream) {
+  if (!(global_scale > 0.0f) || global_scale > 3.0e38f) return PETIT_ERR_INVALID_ARG;
+  return quantize_common(kNVFP4, W, global_scale, w_packed, s_e4m3, n, k, stream);
+}
+
+petit_status_t petit_quantize_mxfp4(const void* W, uint8_t* w_packed, uint8_t* s_e8m0, int64_t n,
+                                    int64_t k, petit_stream_t stream) {
+  return quantize_common(kMXFP4, W, 1.0f, w_packed, s_e8m0, n, k, stream);
+}
+
+static petit_status_t repack_common(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* wo,
+                                    uint8_t* so, int64_t n, int64_t k, petit_stream_t stream) {
+  if (!wp || !sp || !wo || !so) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (!aligned16(wp) || !aligned16(sp) || !aligned16(wo) || !aligned16(so))
+    return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(
+      petit::launch_repack(fmt, wp, sp, wo, so, n, k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3, uint8_t* w_out,
+                                  uint8_t* s_out, int64_t n, int64_t k, petit_stream_t stream) {
+  return repack_common(kNVFP4, w_packed, s_e4m3, w_out, s_out, n, k, stream);
+}
+
+petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0, uint8_t* w_out,
+                                  uint8_t* s_out, int64_t n, int64_t k, petit_stream_t stream) {
+  return repack_common(kMXFP4, w_packed, s_e8m0, w_out, s_out, n, k, stream);
+}
+
+petit_status_t petit_dequant_bf16(const uint8_t* w_rep, const uint8_t* s_rep, int fmt,
+                                  void* W_out, int64_t n, int64_t k, petit_stream_t stream) {
+  if (!w_rep || !s_rep || !W_out) return PETIT_ERR_INVALID_ARG;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (!aligned16(w_rep) || !aligned16(s_rep) || !aligned16(W_out)) return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(petit::launch_dequant(fmt, w_rep, s_rep, W_out, n, k,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* w_rep, const uint8_t* s_rep,
+                                     float global_scale, void* C, int64_t m, int64_t n, int64_t k,
+                                     void* workspace, size_t workspace_bytes,
+                                     petit_stream_t stream) {
+  if (!(global_scale > 0.0f) || global_scale > 1.0e36f) return PETIT_ERR_INVALID_ARG;
+  // the register decode yields Wq * 2^-8; the epilogue restores it with g
+  return gemm_common(kNVFP4, A, w_rep, s_rep, global_scale * 256.0f, C, m, n, k, workspace,
+                     workspace_bytes, stream);
+}
+
+petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* w_rep, const uint8_t* s_rep,
+                                     void* C, int64_t m, int64_t n, int64_t k, void* workspace,
+                                     size_t workspace_bytes, petit_stream_t stream) {
+  return gemm_common(kMXFP4, A, w_rep, s_rep, 1.0f, C, m, n, k, workspace, workspace_bytes,
+                     stream);
+}
+
+petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream) {
+  if (!workspace) return PETIT_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return PETIT_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PETIT_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PETIT_ERR_CUDA;
+  if (word == 0) return PETIT_OK;
+  if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return PETIT_ERR_CUDA;
+  return (word & petit::kStatusTimeout) ? PETIT_ERR_TIMEOUT : PETIT_ERR_CUDA;
+}
+
+petit_status_t petit_selftest_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                      petit_stream_t stream) {
+  if (!workspace || timeout_us < 1 || timeout_us > 1000000u) return PETIT_ERR_INVALID_ARG;
+  if (workspace_bytes < petit::kWsHeaderBytes) return PETIT_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(petit::launch_selftest_timeout(static_cast<uint32_t*>(workspace),
+                                                  uint64_t(timeout_us) * 1000ull,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// Repacked weight layout and the in-register FP4 -> BF16 decode shared by the
+// repack, dequant-hook and GEMM kernels.
+//
+// The decode turns an E2M1 code into BF16 with shifts and masks only (the
+// pages' "dequantise in registers with bit tricks"; Petit blog, "Efficient
+// dequantization via preprocessing", where an offline shuffle puts the bits
+// where the decode wants them).  Placing a code's two exponent bits on the two
+// lowest BF16 exponent bits and its mantissa bit on the top BF16 mantissa bit
+// gives the BF16 number value(code) * 2^-126 exactly -- including code 0.5,
+// which becomes the BF16 subnormal 2^-127.  One BF16x2 multiply by the block
+// scale (pre-multiplied by 2^118, exact for every E4M3 value) then yields
+// value * scale * 2^-8, exactly representable; the GEMM epilogue multiplies
+// the FP32 sum by g * 2^8.  MXFP4 uses two exact multiplies (by 2^126, then by
+// the E8M0 scale) because E8M0 covers 2^-127..2^127.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace petit {
+
+constexpr int kLayoutVersion = 1;
+constexpr int kTileN = 128;   // weight rows per tile (the MMA M side)
+constexpr int kStageK = 128;  // k elements per repacked chunk / pipeline stage
+constexpr int kWChunkBytes = kTileN * kStageK / 2;  // 8192
+constexpr int kGroupsPerRow = kStageK / 32;         // 16-byte groups per row per chunk
+
+enum : int { kNVFP4 = 0, kMXFP4 = 1 };
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<kNVFP4> {
+  static constexpr int kBlock = 16;                          // k per scale
+  static constexpr int kSChunkBytes = kTileN * kStageK / 16; // 1024
+  static constexpr int kScaleBytesPerHalf = 4;               // 64 k / 16
+};
+template <>
+struct FmtTraits<kMXFP4> {
+  static constexpr int kBlock = 32;
+  static constexpr int kSChunkBytes = kTileN * kStageK / 32; // 512
+  static constexpr int kScaleBytesPerHalf = 2;               // 64 k / 32
+};
+
+// ---------------------------------------------------------------- layout
+// Weights: chunk (tile t, stage s) starts at byte (t * stages + s) * 8192.
+// Inside a chunk, the 16-byte group g (k = 32g .. 32g+31 of the stage) of row
+// r (0..127) sits at byte (g * 128 + r) * 16, so a warp reading one group for
+// 32 consecutive rows touches 512 consecutive bytes (no bank conflicts).
+// Word w of a group holds k = 8w .. 8w+7 in the bit order of pack_word().
+//
+// Scales: chunk (t, s) starts at byte (t * stages + s) * kSChunkBytes; inside,
+// half h (k = 64h .. 64h+63) of row r sits at (h * 128 + r) *
+// kScaleBytesPerHalf, byte j holding block j of that half.
+__host__ __device__ constexpr size_t w_chunk_offset(int64_t tile, int64_t stage,
+                                                    int64_t stages) {
+  return static_cast<size_t>((tile * stages + stage) * kWChunkBytes);
+}
+
+// Bit position of each code's bits (sign, e1, e0, m) in a 32-bit word:
+//   c0: 15  8  7  6     c1: 31 24 23 22     (decode: q & M)
+//   c2: 12  5  4  3     c3: 28 21 20 19     (decode: (q << 3) & M)
+//   c4:  9  2  1  0     c5: 25 18 17 16     (decode: (q << 6) & M)
+//   c6: 11 14 13 10     c7: 27 30 29 26     (decode: three shifts)
+// with M = 0x81C081C0 selecting BF16 bits {15, 8, 7, 6} of both halves.
+__host__ __device__ inline uint32_t pack_word(const uint32_t (&c)[8]) {
+  auto mag = [](uint32_t x) { return x & 7u; };
+  auto sgn = [](uint32_t x) { return (x >> 3) & 1u; };
+  uint32_t q = 0;
+  q |= (mag(c[0]) << 6) | (sgn(c[0]) << 15);
+  q |= (mag(c[1]) << 22) | (sgn(c[1]) << 31);
+  q |= (mag(c[2]) << 3) | (sgn(c[2]) << 12);
+  q |= (mag(c[3]) << 19) | (sgn(c[3]) << 28);
+  q |= (mag(c[4]) << 0) | (sgn(c[4]) << 9);
+  q |= (mag(c[5]) << 16) | (sgn(c[5]) << 25);
+  q |= (((c[6] >> 1) & 3u) << 13) | ((c[6] & 1u) << 10) | (sgn(c[6]) << 11);
+  q |= (((c[7] >> 1) & 3u) << 29) | ((c[7] & 1u) << 26) | (sgn(c[7]) << 27);
+  return q;
+}
+
+// ---------------------------------------------------------------- decode
+// Four BF16x2 words value(c_i) * 2^-126 for the pairs (c0,c1) .. (c6,c7).
+__device__ __forceinline__ void decode_word_raw(uint32_t q, uint32_t (&p)[4]) {
+  constexpr uint32_t M = 0x81C081C0u;
+  p[0] = q & M;
+  p[1] = (q << 3) & M;
+  p[2] = (q << 6) & M;
+  p[3] = ((q >> 6) & 0x01800180u) | ((q >> 4) & 0x00400040u) | ((q << 4) & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_splat_f32(float f) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(f));
+  return d;
+}
+
+// Two E4M3 bytes (low 16 bits of v: byte 0 = first block) -> BF16x2 splats of
+// scale * 2^118.  The hardware E4M3 -> F16 conversion is exact (subnormal
+// scales included); F16 -> F32 is exact; * 2^118 stays below 2^127.
+__device__ __forceinline__ void nv_scale_splats(uint32_t v, uint32_t& s0, uint32_t& s1) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(v & 0xFFFFu)));
+  const float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  const float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+  s0 = bf16x2_splat_f32(f0 * 0x1p118f);
+  s1 = bf16x2_splat_f32(f1 * 0x1p118f);
+}
+
+// E8M0 byte -> BF16x2 splat of 2^(c-127) (c = 0 is the BF16 subnormal 2^-127).
+__device__ __forceinline__ uint32_t mx_scale_splat(uint32_t c) {
+  uint32_t b = (c & 0xFFu) << 7;
+  b = b > 0x40u ? b : 0x40u;
+  return b | (b << 16);
+}
+
+constexpr uint32_t kBf16x2_2p126 = 0x7E807E80u;  // 2^126 in both halves
+constexpr uint32_t kBf16x2_2p8 = 0x43804380u;    // 2^8 in both halves
+
+// Decode one 16-byte group (32 codes) into 16 BF16x2 words: out[j] holds k =
+// 2j (low half) and 2j+1 (high half).  NVFP4: sc holds the two E4M3 bytes of
+// the group (k 0-15, 16-31); result = Wq * 2^-8.  MXFP4: sc holds the E8M0
+// byte; result = Wq.
+template <int FMT>
+__device__ __forceinline__ void decode_group(const uint4& g, uint32_t sc, uint32_t (&out)[16]) {
+  const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+  if constexpr (FMT == kNVFP4) {
+    uint32_t s0, s1;
+    nv_scale_splats(sc, s0, s1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t p[4];
+      decode_word_raw(w[i], p);
+      const uint32_t s = i < 2 ? s0 : s1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) out[4 * i + j] = bmul2(p[j], s);
+    }
+  } else {
+    const uint32_t s = mx_scale_splat(sc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t p[4];
+      decode_word_raw(w[i], p);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) out[4 * i + j] = bmul2(bmul2(p[j], kBf16x2_2p126), s);
+    }
+  }
+}
+
+}  // namespace petit

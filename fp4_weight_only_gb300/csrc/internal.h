@@ -1,0 +1,59 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace petit {
+
+constexpr uint32_t kStatusTimeout = 1u;  // bit in the workspace status word
+
+// Workspace: [0, 256) status word and reserved; then per-tile arrival
+// counters (u32); then FP32 split-K partial slots, two per CTA.
+constexpr size_t kWsHeaderBytes = 256;
+
+struct WsLayout {
+  size_t counters_off;
+  size_t partials_off;
+  size_t total;
+};
+
+struct GemmPlan {
+  int fmt;
+  int bn;          // activation rows per tile (MMA N)
+  int m_tiles;
+  int n_tiles;
+  int k_stages;
+  int64_t units;   // n_tiles * m_tiles * k_stages
+  int num_ctas;
+  WsLayout ws;
+};
+
+GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
+
+struct GemmArgs {
+  const void* A;
+  const uint8_t* w;
+  const uint8_t* s;
+  void* C;
+  int64_t m, n, k;
+  float alpha;
+  uint8_t* workspace;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, const CUtensorMap& tmap_a,
+                        cudaStream_t stream);
+
+cudaError_t launch_absmax(const void* x, int64_t count, float* out, cudaStream_t stream);
+cudaError_t launch_quantize(int fmt, const void* W, float g, uint8_t* wp, uint8_t* sp,
+                            int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* wo,
+                          uint8_t* so, int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_dequant(int fmt, const uint8_t* wr, const uint8_t* sr, void* out,
+                           int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace petit

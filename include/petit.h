@@ -1,0 +1,190 @@
+/*
+ * petit.h -- C ABI of the GB300 (sm_103a) BF16-activation x FP4-weight GEMM.
+ *
+ * The operation (Petit blog "AMD GPU 上 FP4 混合精度推理优化", sections
+ * "Introduction" and "Efficient dequantization via preprocessing"; Petit PyPI
+ * page, "Features"):
+ *
+ *     C[m, n] = g * sum_k A[m, k] * Wq[n, k]        Wq = code * block_scale
+ *
+ *   A   BF16 activations, row-major [m][k].
+ *   W   E2M1 (FP4) codes, two per byte, row-major [n][k/2]; element 2j of a
+ *       row sits in the low nibble of byte j ("FP4 GEMM on Rubin/Blackwell
+ *       with CUTLASS", section 3.3: two FP4 values per byte).
+ *   NVFP4: one E4M3 scale per 16 consecutive k of a row, [n][k/16], and an
+ *       FP32 per-tensor global scale g (Petit blog, "Detailed performance
+ *       analysis": 16 elements share one FP8 scale).
+ *   MXFP4: one E8M0 scale per 32 consecutive k, [n][k/32], g = 1 (Petit PyPI
+ *       page, "Features").
+ *   Accumulation is FP32; C is BF16 (round to nearest even), row-major [m][n].
+ *
+ * Weights are used through an offline "repack" (Petit PyPI page, "Techniques
+ * and performance": weights are shuffled offline, as in Marlin, so the GPU
+ * dequantises cheaply).  The repacked buffers have exactly the byte size of
+ * their inputs and an opaque, versioned order (petit_layout_version()).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device pointers; the caller allocates
+ *     and frees them.  The library never allocates or frees memory and never
+ *     synchronises, except petit_get_device_status().
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) on the current device.
+ *   - Every entry point validates its arguments first; on any error it
+ *     returns a non-zero petit_status_t and enqueues nothing.  No entry point
+ *     aborts, throws or prints.
+ *   - Device pointers must be 16-byte aligned (PETIT_ERR_MISALIGNED).
+ *   - The device must be compute capability 10.3 (GB300, sm_103a)
+ *     (PETIT_ERR_ARCH).
+ */
+#ifndef PETIT_H
+#define PETIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* petit_stream_t; /* same type as cudaStream_t */
+
+typedef enum petit_status {
+  PETIT_OK = 0,
+  PETIT_ERR_INVALID_ARG = 1,       /* null pointer, bad format id, m < 1 ... */
+  PETIT_ERR_UNSUPPORTED_SHAPE = 2, /* n or k not a multiple of 128, too large */
+  PETIT_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
+  PETIT_ERR_WORKSPACE = 4,         /* workspace missing or too small */
+  PETIT_ERR_ARCH = 5,              /* current device is not sm_103 */
+  PETIT_ERR_CUDA = 6,              /* a CUDA runtime call failed */
+  PETIT_ERR_TIMEOUT = 7            /* a bounded device-side wait ran out */
+} petit_status_t;
+
+typedef enum petit_format {
+  PETIT_FMT_NVFP4 = 0, /* E2M1 + E4M3 per 16 + FP32 global scale */
+  PETIT_FMT_MXFP4 = 1  /* E2M1 + E8M0 per 32 */
+} petit_format_t;
+
+/* Version of the repacked weight/scale order.  Stored repacked weights are
+ * only valid for the version that wrote them. */
+int petit_layout_version(void);
+
+/* Static text for a status code (never NULL). */
+const char* petit_status_string(petit_status_t status);
+
+/* ------------------------------------------------------------------ sizes */
+
+/* Bytes of the repacked weight buffer: n*k/2 (same as the packed input). */
+size_t petit_repacked_weight_bytes(int64_t n, int64_t k);
+
+/* Bytes of the repacked scale buffer: n*k/16 (NVFP4) or n*k/32 (MXFP4). */
+size_t petit_repacked_scale_bytes(int64_t n, int64_t k, int fmt);
+
+/* Bytes of GEMM workspace for this problem on the current device (holds a
+ * device status word, per-tile arrival counters and FP32 split-K partials).
+ * Returns 0 if the arguments are invalid or no device is usable.  A
+ * workspace must be zero-filled once after allocation; every successful
+ * GEMM leaves it in that state again, so it can be reused by later calls of
+ * any size that fits. */
+size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt);
+
+/* ------------------------------------------------------ offline weight prep */
+
+/* Largest |x| over `count` BF16 values x (device) -> *amax_out (device FP32).
+ * Used to derive the NVFP4 global scale.  count >= 1. */
+petit_status_t petit_absmax_bf16(const void* x, int64_t count, float* amax_out,
+                                 petit_stream_t stream);
+
+/* NVFP4 global scale from the tensor maximum: amax / (6 * 448), in FP32. */
+float petit_nvfp4_global_scale(float amax);
+
+/* Quantise BF16 weights W [n][k] (device) to NVFP4: for every row and
+ * 16-element block, t = max(amax, 1e-8) / (6 * g) (FP32), scale = E4M3(t)
+ * round-to-nearest-even saturating (a zero result becomes 0x01 so scales are
+ * positive), codes = nearest E2M1 of x / (scale * g), ties to even, no
+ * negative zero.  Block max-abs scaling and the 1e-8 floor follow "FP4 GEMM
+ * on Rubin/Blackwell with CUTLASS", sections 2.2 and 5.2.
+ * Outputs: w_packed [n][k/2], s_e4m3 [n][k/16] (device).  k % 16 == 0. */
+petit_status_t petit_quantize_nvfp4(const void* W, float global_scale,
+                                    uint8_t* w_packed, uint8_t* s_e4m3,
+                                    int64_t n, int64_t k, petit_stream_t stream);
+
+/* Quantise BF16 weights W [n][k] (device) to MXFP4: per 32-element block the
+ * scale is 2^e with e = ceil(log2(max(amax, 1e-8) / 6)) (E8M0 code e + 127,
+ * clamped to [0, 254]); codes are the nearest E2M1 of x / 2^e, ties to even.
+ * Outputs: w_packed [n][k/2], s_e8m0 [n][k/32] (device).  k % 32 == 0. */
+petit_status_t petit_quantize_mxfp4(const void* W, uint8_t* w_packed,
+                                    uint8_t* s_e8m0, int64_t n, int64_t k,
+                                    petit_stream_t stream);
+
+/* Offline repack (Marlin-style shuffle; Petit blog, "Efficient dequantization
+ * via preprocessing"): permutes the packed codes and the scale bytes into the
+ * per-tile, per-pipeline-stage order the GEMM streams, with each 32-bit word
+ * holding its 8 codes in the bit positions the in-register BF16 decode uses.
+ * Inputs w_packed [n][k/2], s_e4m3 [n][k/16] (device, read only); outputs
+ * w_out (petit_repacked_weight_bytes), s_out (petit_repacked_scale_bytes)
+ * (device, must not overlap the inputs).  n % 128 == 0, k % 128 == 0.
+ * Scales must be positive (not 0x00, 0x7F or negative) -- the precondition of
+ * Petit's offline transform (Petit PyPI page, "Known limitations"); the
+ * library does not check them.  Negative-zero codes are harmless here (they
+ * decode to -0.0). */
+petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3,
+                                  uint8_t* w_out, uint8_t* s_out,
+                                  int64_t n, int64_t k, petit_stream_t stream);
+
+/* Same as petit_repack_nvfp4 for MXFP4 scales s_e8m0 [n][k/32] (code 0xFF is
+ * not a number and must not occur). */
+petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0,
+                                  uint8_t* w_out, uint8_t* s_out,
+                                  int64_t n, int64_t k, petit_stream_t stream);
+
+/* Test hook: dequantise repacked weights with the GEMM's own device decode
+ * routine and write Wq = code * block_scale as BF16, row-major [n][k]
+ * (device).  The global scale is not applied.  Wq is exactly representable,
+ * so the result is bit-exact.  (The per-block dump suggested as a debugging
+ * aid in "FP4 GEMM on Rubin/Blackwell with CUTLASS", section 7.) */
+petit_status_t petit_dequant_bf16(const uint8_t* w_rep, const uint8_t* s_rep,
+                                  int fmt, void* W_out, int64_t n, int64_t k,
+                                  petit_stream_t stream);
+
+/* --------------------------------------------------------------- the GEMM */
+
+/* C[m][n] = bf16(g * sum_k A[m][k] * Wq[n][k]) with FP32 accumulation.
+ * A: BF16 [m][k] (device); w_rep / s_rep: repacked NVFP4 weights and E4M3
+ * scales (device); C: BF16 [m][n] (device, must not overlap A);
+ * workspace: at least petit_gemm_workspace_bytes(m, n, k, PETIT_FMT_NVFP4)
+ * zero-filled bytes (device).  m >= 1 (any value); n % 128 == 0;
+ * k % 128 == 0.  Calls that share a workspace must not run concurrently.
+ * Device-side waits are bounded: if one runs out, the kernel stops early,
+ * C is not valid, and petit_get_device_status() reports PETIT_ERR_TIMEOUT. */
+petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* w_rep,
+                                     const uint8_t* s_rep, float global_scale,
+                                     void* C, int64_t m, int64_t n, int64_t k,
+                                     void* workspace, size_t workspace_bytes,
+                                     petit_stream_t stream);
+
+/* Same with repacked MXFP4 weights and E8M0 scales (no global scale). */
+petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* w_rep,
+                                     const uint8_t* s_rep, void* C,
+                                     int64_t m, int64_t n, int64_t k,
+                                     void* workspace, size_t workspace_bytes,
+                                     petit_stream_t stream);
+
+/* --------------------------------------------------------- error reporting */
+
+/* Waits for `stream`, reads the status word the kernels keep at the start of
+ * `workspace` and clears it.  Returns PETIT_OK, PETIT_ERR_TIMEOUT (a bounded
+ * wait ran out in some earlier call on this workspace) or PETIT_ERR_CUDA. */
+petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream);
+
+/* Fault-detection self test: launches one CTA that waits on a barrier nobody
+ * arrives at, with a limit of `timeout_us` microseconds (1..10^6).  The wait
+ * runs out, the kernel records PETIT_ERR_TIMEOUT in the workspace status
+ * word and returns; the CUDA context stays usable.  workspace_bytes >= 256. */
+petit_status_t petit_selftest_timeout(void* workspace, size_t workspace_bytes,
+                                      uint32_t timeout_us, petit_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PETIT_H */

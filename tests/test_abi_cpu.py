@@ -1,0 +1,94 @@
+"""C-ABI library: builds, loads without a GPU, exports every declared symbol,
+and rejects bad arguments before touching the device (no compute calls)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp4_weight_only_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "petit.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(petit_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("petit_repack_nvfp4", "petit_repack_mxfp4", "petit_gemm_bf16_nvfp4",
+                     "petit_gemm_bf16_mxfp4", "petit_dequant_bf16", "petit_gemm_workspace_bytes",
+                     "petit_get_device_status", "petit_layout_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) == set(binding.SIGNATURES), "binding signatures out of date with the header"
+
+
+def test_host_only_entry_points(lib):
+    assert lib.petit_layout_version() >= 1
+    for s in range(8):
+        assert lib.petit_status_string(s)
+    assert lib.petit_status_string(99) == b"unknown status"
+    assert lib.petit_repacked_weight_bytes(8192, 8192) == 8192 * 4096
+    assert lib.petit_repacked_scale_bytes(8192, 8192, 0) == 8192 * 512
+    assert lib.petit_repacked_scale_bytes(8192, 8192, 1) == 8192 * 256
+    assert lib.petit_repacked_scale_bytes(8192, 8192, 7) == 0
+    assert lib.petit_nvfp4_global_scale(ctypes.c_float(2688.0)) == 1.0
+
+
+P = ctypes.c_void_p
+
+
+def test_argument_validation_without_gpu(lib):
+    a = P(0x10000)        # aligned fake addresses: validation must reject before any use
+    bad = P(0x10008)
+    NULL = P(0)
+    s = P(0)
+    # null pointer / m < 1
+    assert lib.petit_gemm_bf16_nvfp4(NULL, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
+    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 0, 1024, 1024, a, 1 << 20, s) == 1
+    assert lib.petit_gemm_bf16_nvfp4(a, a, a, -1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
+    # shapes: n, k multiples of 128
+    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 16, 1000, 1024, a, 1 << 20, s) == 2
+    assert lib.petit_gemm_bf16_mxfp4(a, a, a, a, 16, 1024, 1056, a, 1 << 20, s) == 2
+    # alignment
+    assert lib.petit_gemm_bf16_nvfp4(bad, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 3
+    # workspace missing
+    assert lib.petit_gemm_bf16_mxfp4(a, a, a, a, 16, 1024, 1024, NULL, 0, s) == 4
+    assert lib.petit_repack_nvfp4(a, a, a, a, 100, 1024, s) == 2
+    assert lib.petit_repack_mxfp4(a, NULL, a, a, 128, 128, s) == 1
+    assert lib.petit_dequant_bf16(a, a, 5, a, 128, 128, s) == 1
+    assert lib.petit_quantize_nvfp4(a, ctypes.c_float(0.0), a, a, 4, 32, s) == 1
+    assert lib.petit_quantize_mxfp4(a, a, a, 4, 48, s) == 2
+    assert lib.petit_absmax_bf16(a, 0, a, s) == 1
+    assert lib.petit_selftest_timeout(a, 16, 100, s) == 4
+    assert lib.petit_selftest_timeout(a, 256, 0, s) == 1
+    assert lib.petit_get_device_status(NULL, s) == 1
+    # sizes are 0 for invalid shapes
+    assert lib.petit_gemm_workspace_bytes(16, 1000, 1024, 0) == 0
+    assert lib.petit_gemm_workspace_bytes(0, 1024, 1024, 0) == 0
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a = P(0x10000)
+    # valid arguments, but no usable device: a CUDA error status, never a crash
+    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 30, P(0)) == 6
+    assert lib.petit_gemm_workspace_bytes(16, 1024, 1024, 0) == 0
