@@ -45,6 +45,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--profile-only", action="store_true",
+                   help="prepare one weight set and launch each decode GEMM once (for ncu captures)")
+    p.add_argument("--profile-m", type=int, default=M_DECODE)
     return p.parse_args()
 
 
@@ -216,7 +219,7 @@ def run_ours(args, rank, world, local):
         fw = binding.FP4Weight(w, "nvfp4", 1.0)
         del w
         sets[0].append(fw)
-        sets[1].append((fw.w_rep.clone(), fw.s_rep.clone()))
+        sets[1].append(fw.rep.clone())
         acts.append(synth.activations(M_DECODE, k, seed=200 + i, device=dev))
         outs.append(torch.empty((M_DECODE, n), dtype=torch.bfloat16, device=dev))
     ws = binding.Workspace(dev)
@@ -226,8 +229,8 @@ def run_ours(args, rank, world, local):
 
     def launch(i, which, m=M_DECODE, a=None, c=None):
         fw = sets[0][i]
-        wr, sr = (fw.w_rep, fw.s_rep) if which == 0 else sets[1][i]
-        binding.gemm(acts[i] if a is None else a, wr, sr, fw.n, "nvfp4", 1.0, workspace=ws,
+        rep = fw.rep if which == 0 else sets[1][i]
+        binding.gemm(acts[i] if a is None else a, rep, fw.n, "nvfp4", 1.0, workspace=ws,
                      out=outs[i] if c is None else c)
 
     # one CUDA graph per (GEMM, weight copy)
@@ -315,8 +318,8 @@ def run_ours(args, rank, world, local):
         for i, (name, n, k) in enumerate(SHAPES):
             a_dev[i].copy_(a_host[i], non_blocking=True)
             fw = sets[0][i]
-            wr, sr = (fw.w_rep, fw.s_rep) if (s & 1) == 0 else sets[1][i]
-            c = binding.gemm(a_dev[i], wr, sr, n, "nvfp4", 1.0, workspace=ws)
+            rep = fw.rep if (s & 1) == 0 else sets[1][i]
+            c = binding.gemm(a_dev[i], rep, n, "nvfp4", 1.0, workspace=ws)
             c_host[i].copy_(c, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -396,8 +399,32 @@ def run_ours(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def run_profile_only(args, local):
+    """Quantise + repack the four weights, then launch each GEMM once:
+    launch order qkv, o, gate_up, down (gemm_kernel launches 0..3)."""
+    from fp4_weight_only_gb300 import binding, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load()
+    ws = binding.Workspace(dev)
+    m = args.profile_m
+    for i, (name, n, k) in enumerate(SHAPES):
+        w = synth.weights(n, k, seed=100 + i, device=dev)
+        fw = binding.FP4Weight(w, "nvfp4", 1.0)
+        del w
+        a = synth.activations(m, k, seed=200 + i, device=dev)
+        fw(a, workspace=ws)
+        torch.cuda.synchronize()
+        del fw
+    assert ws.status() == 0
+    print(f"profile-only: m={m} launched {len(SHAPES)} GEMMs", flush=True)
+
+
 def main():
     args = parse()
+    if args.profile_only:
+        return run_profile_only(args, dist_env()[2])
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist

@@ -40,20 +40,19 @@ _c_sz = ctypes.c_size_t
 SIGNATURES = {
     "petit_layout_version": (ctypes.c_int, []),
     "petit_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-    "petit_repacked_weight_bytes": (_c_sz, [_c_i64, _c_i64]),
-    "petit_repacked_scale_bytes": (_c_sz, [_c_i64, _c_i64, ctypes.c_int]),
+    "petit_repacked_bytes": (_c_sz, [_c_i64, _c_i64, ctypes.c_int]),
     "petit_gemm_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, ctypes.c_int]),
     "petit_absmax_bf16": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p]),
     "petit_nvfp4_global_scale": (ctypes.c_float, [ctypes.c_float]),
     "petit_quantize_nvfp4": (ctypes.c_int, [_c_p, ctypes.c_float, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
     "petit_quantize_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
-    "petit_repack_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
-    "petit_repack_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
-    "petit_dequant_bf16": (ctypes.c_int, [_c_p, _c_p, ctypes.c_int, _c_p, _c_i64, _c_i64, _c_p]),
-    "petit_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64,
-                                             _c_i64, _c_p, _c_sz, _c_p]),
-    "petit_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p,
-                                             _c_sz, _c_p]),
+    "petit_repack_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_repack_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_dequant_bf16": (ctypes.c_int, [_c_p, ctypes.c_int, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
+                                             _c_p, _c_sz, _c_p]),
+    "petit_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_sz,
+                                             _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
 }
@@ -136,25 +135,23 @@ def quantize(W, fmt="nvfp4", global_scale=1.0):
 
 
 def repack(w_packed, scales, fmt="nvfp4"):
-    """Packed codes [n, k/2] + scales -> repacked (weights, scales) uint8."""
+    """Packed codes [n, k/2] + scales -> one repacked uint8 buffer."""
     _need(w_packed, torch.uint8, "w_packed")
     _need(scales, torch.uint8, "scales")
     n, half_k = w_packed.shape
     k = half_k * 2
     L = load()
-    wo = torch.empty(L.petit_repacked_weight_bytes(n, k), dtype=torch.uint8, device=w_packed.device)
-    so = torch.empty(max(L.petit_repacked_scale_bytes(n, k, FORMATS[fmt]), 1), dtype=torch.uint8,
-                     device=w_packed.device)
+    out = torch.empty(max(L.petit_repacked_bytes(n, k, FORMATS[fmt]), 1), dtype=torch.uint8,
+                      device=w_packed.device)
     fn = L.petit_repack_nvfp4 if fmt == "nvfp4" else L.petit_repack_mxfp4
-    _check(fn(_ptr(w_packed), _ptr(scales), _ptr(wo), _ptr(so), n, k, _stream()), "repack_" + fmt)
-    return wo, so
+    _check(fn(_ptr(w_packed), _ptr(scales), _ptr(out), n, k, _stream()), "repack_" + fmt)
+    return out
 
 
-def dequant(w_rep, s_rep, n, k, fmt="nvfp4"):
+def dequant(rep, n, k, fmt="nvfp4"):
     """Repacked weights -> BF16 Wq [n, k] (test hook; bit-exact)."""
-    out = torch.empty((n, k), dtype=torch.bfloat16, device=w_rep.device)
-    _check(load().petit_dequant_bf16(_ptr(w_rep), _ptr(s_rep), FORMATS[fmt], _ptr(out), n, k, _stream()),
-           "dequant")
+    out = torch.empty((n, k), dtype=torch.bfloat16, device=rep.device)
+    _check(load().petit_dequant_bf16(_ptr(rep), FORMATS[fmt], _ptr(out), n, k, _stream()), "dequant")
     return out
 
 
@@ -179,7 +176,7 @@ class Workspace:
         return load().petit_get_device_status(_ptr(self.buf), _stream())
 
 
-def gemm(A, w_rep, s_rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
+def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
     """C[m, n] = g * A @ dequant(W)^T in BF16 (FP32 accumulation)."""
     _need(A, torch.bfloat16, "A")
     m, k = A.shape
@@ -191,11 +188,11 @@ def gemm(A, w_rep, s_rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=
     C = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=A.device)
     L = load()
     if fmt == "nvfp4":
-        st = L.petit_gemm_bf16_nvfp4(_ptr(A), _ptr(w_rep), _ptr(s_rep), ctypes.c_float(global_scale), _ptr(C),
+        st = L.petit_gemm_bf16_nvfp4(_ptr(A), _ptr(rep), ctypes.c_float(global_scale), _ptr(C),
                                      m, n, k, _ptr(buf), buf.numel(), _stream())
     else:
-        st = L.petit_gemm_bf16_mxfp4(_ptr(A), _ptr(w_rep), _ptr(s_rep), _ptr(C), m, n, k, _ptr(buf),
-                                     buf.numel(), _stream())
+        st = L.petit_gemm_bf16_mxfp4(_ptr(A), _ptr(rep), _ptr(C), m, n, k, _ptr(buf), buf.numel(),
+                                     _stream())
     _check(st, "gemm_" + fmt)
     return C
 
@@ -219,8 +216,8 @@ class FP4Weight:
             self.global_scale = float(global_scale)
         else:
             self.global_scale = 1.0
-        self.w_packed, self.scales = quantize(W, fmt, self.global_scale)
-        self.w_rep, self.s_rep = repack(self.w_packed, self.scales, fmt)
+        w_packed, scales = quantize(W, fmt, self.global_scale)
+        self.rep = repack(w_packed, scales, fmt)
 
     def __call__(self, A, workspace=None, out=None):
-        return gemm(A, self.w_rep, self.s_rep, self.n, self.fmt, self.global_scale, workspace, out)
+        return gemm(A, self.rep, self.n, self.fmt, self.global_scale, workspace, out)

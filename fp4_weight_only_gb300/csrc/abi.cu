@@ -75,15 +75,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A [m][k] BF16, boxes of 64 k x bn rows, 128-byte swizzle, zero fill outside.
-petit_status_t encode_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t k, int bn) {
+// A [m][k] BF16 viewed as [k/64 slabs][m rows][64 k]: one box brings 2*ku
+// slabs of 64 k for bn rows (128-byte swizzle, zero fill for rows >= m), i.e.
+// a whole pipeline unit's activations in one request.
+petit_status_t encode_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t k, int bn,
+                            int ku) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return PETIT_ERR_CUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bn)};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(k / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bn), static_cast<cuuint32_t>(2 * ku)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PETIT_OK : PETIT_ERR_CUDA;
@@ -96,13 +99,13 @@ petit_status_t check_tiled_shape(int64_t n, int64_t k) {
   return PETIT_OK;
 }
 
-petit_status_t gemm_common(int fmt, const void* A, const uint8_t* w, const uint8_t* s,
-                           float alpha, void* C, int64_t m, int64_t n, int64_t k, void* ws,
-                           size_t ws_bytes, petit_stream_t stream) {
-  if (!A || !w || !s || !C || m < 1) return PETIT_ERR_INVALID_ARG;
+petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alpha, void* C,
+                           int64_t m, int64_t n, int64_t k, void* ws, size_t ws_bytes,
+                           petit_stream_t stream) {
+  if (!A || !rep || !C || m < 1) return PETIT_ERR_INVALID_ARG;
   if (petit_status_t st = check_tiled_shape(n, k)) return st;
   if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(A) || !aligned16(w) || !aligned16(s) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
+  if (!aligned16(A) || !aligned16(rep) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
   if (!ws) return PETIT_ERR_WORKSPACE;
   if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
   int sms = 0;
@@ -111,8 +114,8 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* w, const uint8
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn)) return st;
-  petit::GemmArgs args{A, w, s, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
+  petit::GemmArgs args{A, rep, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
   return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -136,15 +139,11 @@ const char* petit_status_string(petit_status_t s) {
   return "unknown status";
 }
 
-size_t petit_repacked_weight_bytes(int64_t n, int64_t k) {
+size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt) {
   if (n < 0 || k < 0) return 0;
-  return static_cast<size_t>(n) * static_cast<size_t>(k) / 2;
-}
-
-size_t petit_repacked_scale_bytes(int64_t n, int64_t k, int fmt) {
-  if (n < 0 || k < 0) return 0;
-  if (fmt == PETIT_FMT_NVFP4) return static_cast<size_t>(n) * static_cast<size_t>(k) / 16;
-  if (fmt == PETIT_FMT_MXFP4) return static_cast<size_t>(n) * static_cast<size_t>(k) / 32;
+  const size_t nk = static_cast<size_t>(n) * static_cast<size_t>(k);
+  if (fmt == PETIT_FMT_NVFP4) return nk / 2 + nk / 16;
+  if (fmt == PETIT_FMT_MXFP4) return nk / 2 + nk / 32;
   return 0;
 }
 
@@ -190,53 +189,50 @@ petit_status_t petit_quantize_mxfp4(const void* W, uint8_t* w_packed, uint8_t* s
   return quantize_common(kMXFP4, W, 1.0f, w_packed, s_e8m0, n, k, stream);
 }
 
-static petit_status_t repack_common(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* wo,
-                                    uint8_t* so, int64_t n, int64_t k, petit_stream_t stream) {
-  if (!wp || !sp || !wo || !so) return PETIT_ERR_INVALID_ARG;
+static petit_status_t repack_common(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* out,
+                                    int64_t n, int64_t k, petit_stream_t stream) {
+  if (!wp || !sp || !out) return PETIT_ERR_INVALID_ARG;
   if (petit_status_t st = check_tiled_shape(n, k)) return st;
-  if (!aligned16(wp) || !aligned16(sp) || !aligned16(wo) || !aligned16(so))
-    return PETIT_ERR_MISALIGNED;
+  if (!aligned16(wp) || !aligned16(sp) || !aligned16(out)) return PETIT_ERR_MISALIGNED;
   if (petit_status_t st = current_device(nullptr)) return st;
   return from_cuda(
-      petit::launch_repack(fmt, wp, sp, wo, so, n, k, reinterpret_cast<cudaStream_t>(stream)));
+      petit::launch_repack(fmt, wp, sp, out, n, k, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3, uint8_t* w_out,
-                                  uint8_t* s_out, int64_t n, int64_t k, petit_stream_t stream) {
-  return repack_common(kNVFP4, w_packed, s_e4m3, w_out, s_out, n, k, stream);
+petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3, uint8_t* rep_out,
+                                  int64_t n, int64_t k, petit_stream_t stream) {
+  return repack_common(kNVFP4, w_packed, s_e4m3, rep_out, n, k, stream);
 }
 
-petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0, uint8_t* w_out,
-                                  uint8_t* s_out, int64_t n, int64_t k, petit_stream_t stream) {
-  return repack_common(kMXFP4, w_packed, s_e8m0, w_out, s_out, n, k, stream);
+petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0, uint8_t* rep_out,
+                                  int64_t n, int64_t k, petit_stream_t stream) {
+  return repack_common(kMXFP4, w_packed, s_e8m0, rep_out, n, k, stream);
 }
 
-petit_status_t petit_dequant_bf16(const uint8_t* w_rep, const uint8_t* s_rep, int fmt,
-                                  void* W_out, int64_t n, int64_t k, petit_stream_t stream) {
-  if (!w_rep || !s_rep || !W_out) return PETIT_ERR_INVALID_ARG;
+petit_status_t petit_dequant_bf16(const uint8_t* rep, int fmt, void* W_out, int64_t n, int64_t k,
+                                  petit_stream_t stream) {
+  if (!rep || !W_out) return PETIT_ERR_INVALID_ARG;
   if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return PETIT_ERR_INVALID_ARG;
   if (petit_status_t st = check_tiled_shape(n, k)) return st;
-  if (!aligned16(w_rep) || !aligned16(s_rep) || !aligned16(W_out)) return PETIT_ERR_MISALIGNED;
+  if (!aligned16(rep) || !aligned16(W_out)) return PETIT_ERR_MISALIGNED;
   if (petit_status_t st = current_device(nullptr)) return st;
-  return from_cuda(petit::launch_dequant(fmt, w_rep, s_rep, W_out, n, k,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(
+      petit::launch_dequant(fmt, rep, W_out, n, k, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* w_rep, const uint8_t* s_rep,
-                                     float global_scale, void* C, int64_t m, int64_t n, int64_t k,
-                                     void* workspace, size_t workspace_bytes,
-                                     petit_stream_t stream) {
+petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* rep, float global_scale,
+                                     void* C, int64_t m, int64_t n, int64_t k, void* workspace,
+                                     size_t workspace_bytes, petit_stream_t stream) {
   if (!(global_scale > 0.0f) || global_scale > 1.0e36f) return PETIT_ERR_INVALID_ARG;
   // the register decode yields Wq * 2^-8; the epilogue restores it with g
-  return gemm_common(kNVFP4, A, w_rep, s_rep, global_scale * 256.0f, C, m, n, k, workspace,
+  return gemm_common(kNVFP4, A, rep, global_scale * 256.0f, C, m, n, k, workspace,
                      workspace_bytes, stream);
 }
 
-petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* w_rep, const uint8_t* s_rep,
-                                     void* C, int64_t m, int64_t n, int64_t k, void* workspace,
+petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C, int64_t m,
+                                     int64_t n, int64_t k, void* workspace,
                                      size_t workspace_bytes, petit_stream_t stream) {
-  return gemm_common(kMXFP4, A, w_rep, s_rep, 1.0f, C, m, n, k, workspace, workspace_bytes,
-                     stream);
+  return gemm_common(kMXFP4, A, rep, 1.0f, C, m, n, k, workspace, workspace_bytes, stream);
 }
 
 petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream) {

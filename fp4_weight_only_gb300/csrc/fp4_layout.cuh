@@ -20,7 +20,7 @@
 
 namespace petit {
 
-constexpr int kLayoutVersion = 1;
+constexpr int kLayoutVersion = 2;
 constexpr int kTileN = 128;   // weight rows per tile (the MMA M side)
 constexpr int kStageK = 128;  // k elements per repacked chunk / pipeline stage
 constexpr int kWChunkBytes = kTileN * kStageK / 2;  // 8192
@@ -35,27 +35,32 @@ struct FmtTraits<kNVFP4> {
   static constexpr int kBlock = 16;                          // k per scale
   static constexpr int kSChunkBytes = kTileN * kStageK / 16; // 1024
   static constexpr int kScaleBytesPerHalf = 4;               // 64 k / 16
+  static constexpr int kChunkBytes = kWChunkBytes + kSChunkBytes;  // 9216
 };
 template <>
 struct FmtTraits<kMXFP4> {
   static constexpr int kBlock = 32;
   static constexpr int kSChunkBytes = kTileN * kStageK / 32; // 512
   static constexpr int kScaleBytesPerHalf = 2;               // 64 k / 32
+  static constexpr int kChunkBytes = kWChunkBytes + kSChunkBytes;  // 8704
 };
 
 // ---------------------------------------------------------------- layout
-// Weights: chunk (tile t, stage s) starts at byte (t * stages + s) * 8192.
-// Inside a chunk, the 16-byte group g (k = 32g .. 32g+31 of the stage) of row
-// r (0..127) sits at byte (g * 128 + r) * 16, so a warp reading one group for
+// One repacked buffer holds, for every (tile t of 128 rows, stage s of 128
+// k), a chunk of kChunkBytes at byte (t * stages + s) * kChunkBytes: 8192
+// bytes of codes followed by the chunk's scales, so one contiguous bulk copy
+// brings both (and consecutive stages of a tile are adjacent, so a copy may
+// span several chunks).
+// Codes: the 16-byte group g (k = 32g .. 32g+31 of the stage) of row r
+// (0..127) sits at byte (g * 128 + r) * 16, so a warp reading one group for
 // 32 consecutive rows touches 512 consecutive bytes (no bank conflicts).
 // Word w of a group holds k = 8w .. 8w+7 in the bit order of pack_word().
-//
-// Scales: chunk (t, s) starts at byte (t * stages + s) * kSChunkBytes; inside,
-// half h (k = 64h .. 64h+63) of row r sits at (h * 128 + r) *
-// kScaleBytesPerHalf, byte j holding block j of that half.
-__host__ __device__ constexpr size_t w_chunk_offset(int64_t tile, int64_t stage,
-                                                    int64_t stages) {
-  return static_cast<size_t>((tile * stages + stage) * kWChunkBytes);
+// Scales (at byte 8192 of the chunk): half h (k = 64h .. 64h+63) of row r
+// sits at (h * 128 + r) * kScaleBytesPerHalf, byte j holding block j of that
+// half.
+template <int FMT>
+__host__ __device__ constexpr size_t chunk_offset(int64_t tile, int64_t stage, int64_t stages) {
+  return static_cast<size_t>((tile * stages + stage) * FmtTraits<FMT>::kChunkBytes);
 }
 
 // Bit position of each code's bits (sign, e1, e0, m) in a 32-bit word:

@@ -15,10 +15,14 @@
 //   partial tiles, whose FP32 partial sums go to the workspace.  The last CTA
 //   to finish a shared tile (atomic arrival counter, no waiting) adds the
 //   partials in a fixed order and writes C, so results are deterministic.
+// * A pipeline unit is KU (1 or 2) consecutive 128-k chunks of one tile.
+//   Its data arrives with exactly two copies: one bulk copy of the repacked
+//   codes + scales (contiguous) and one 3-D TMA box holding all 2*KU 64-k
+//   slabs of A.  The TMA unit of an SM sustains only a limited number of
+//   requests per microsecond, so few large requests keep HBM busy.
 // * Warp roles:
-//     warp 0      producer: bulk copies of the repacked FP4 chunk and its
-//                 scales, and two 2-D TMA boxes of A (128-byte swizzle), into
-//                 a ring of shared-memory stages (mbarrier full/empty);
+//     warp 0      producer: the two copies per unit into a ring of
+//                 shared-memory stages (mbarrier full/empty);
 //     warp 1      tensor-memory owner and MMA issuer (one thread);
 //     warps 2-5   epilogue: tensor memory -> registers -> C or partials;
 //     warps 6-13  dequantisers: shared memory -> registers -> BF16 -> tensor
@@ -44,39 +48,41 @@ constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;    // warps 2..5
 constexpr int kDeqWarp0 = 6;    // warps 6..13
 constexpr int kNumDeqWarps = 8;
-constexpr int kNumABufs = 4;    // dequantised-weight buffers in tensor memory
-constexpr int kAColsPerBuf = kStageK / 2;  // 64 columns of BF16x2 per stage
-constexpr int kDColBase = kNumABufs * kAColsPerBuf;  // 256
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
-  const uint8_t* w;
-  const uint8_t* s;
+  const uint8_t* rep;
   __nv_bfloat16* c;
   float* partials;
   uint32_t* counters;
   uint32_t* status;
   int32_t m, n;
-  int32_t m_tiles, k_stages;
+  int32_t m_tiles, k_units;   // units per tile row = k / (128 * KU)
   int64_t units;
   int32_t num_ctas;
   float alpha;
   uint64_t timeout_ns;
 };
 
-template <int FMT, int BN>
+template <int FMT, int BN, int KU>
 struct Cfg {
-  static constexpr int kAHalfBytes = BN * 128;           // 64 k x BN rows, swizzled
-  static constexpr int kABytes = 2 * kAHalfBytes;
-  static constexpr int kSBytes = FmtTraits<FMT>::kSChunkBytes;
-  static constexpr int kStageBytes = kABytes + kWChunkBytes + kSBytes;
+  using T = FmtTraits<FMT>;
+  static constexpr int kAHalfBytes = BN * 128;                 // one 64-k slab, BN rows
+  static constexpr int kABytes = 2 * KU * kAHalfBytes;
+  static constexpr int kWBytes = KU * T::kChunkBytes;          // codes + scales
+  static constexpr int kStageBytes = kABytes + kWBytes;
   static constexpr int kStages0 = (212 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   static constexpr int kTx = kStageBytes;
-  static constexpr int kNumD = 2;                        // accumulator buffers
+  static constexpr int kNumD = 2;                              // accumulator buffers
+  static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
+  static constexpr int kNumA0 = (static_cast<int>(kTmemCols) - kNumD * BN) / kAColsPerUnit;
+  static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
+  static constexpr int kDColBase = kNumA * kAColsPerUnit;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
+  static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kNumD * BN <= static_cast<int>(kTmemCols), "tensor memory");
   static_assert(kStages >= 2, "pipeline depth");
 };
@@ -87,22 +93,22 @@ __device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t P) 
   return ((u + 1) * P + U - 1) / U - 1;
 }
 
-template <int FMT, int BN>
+template <int FMT, int BN, int KU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_a) {
-  using C = Cfg<FMT, BN>;
+  using C = Cfg<FMT, BN, KU>;
+  using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sm_a = smem;
-  uint8_t* sm_w = sm_a + C::kStages * C::kABytes;
-  uint8_t* sm_s = sm_w + C::kStages * kWChunkBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm_s + C::kStages * C::kSBytes);
+  uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][BN][128 B]
+  uint8_t* sm_w = sm_a + C::kStages * C::kABytes;          // [stage][KU chunks]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kStages * C::kWBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + C::kStages;
   uint64_t* afull = empty + C::kStages;
-  uint64_t* aempty = afull + kNumABufs;
-  uint64_t* dfull = aempty + kNumABufs;
+  uint64_t* aempty = afull + C::kNumA;
+  uint64_t* dfull = aempty + C::kNumA;
   uint64_t* dempty = dfull + C::kNumD;
   uint64_t* fin = dempty + C::kNumD;
   uint64_t* epi_bar = fin + 1;
@@ -117,14 +123,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t cta = blockIdx.x;
   const int64_t u0 = cta * U / P;
   const int64_t u1 = (cta + 1) * U / P;
-  const int64_t KS = p.k_stages;
+  const int64_t KS = p.k_units;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), kNumDeqWarps + 1);
     }
-    for (int i = 0; i < kNumABufs; ++i) {
+    for (int i = 0; i < C::kNumA; ++i) {
       mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
       mbar_init(smem_u32(&aempty[i]), 1);
     }
@@ -167,19 +173,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = static_cast<int>(issued % C::kStages);
         const uint32_t ph = static_cast<uint32_t>((issued / C::kStages) & 1);
         if (!wait(&empty[st], ph ^ 1u)) break;
-        const int64_t tile = u / KS, ks = u % KS;
+        const int64_t tile = u / KS, ku = u % KS;
         const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
         const uint32_t fb = smem_u32(&full[st]);
         mbar_arrive_expect_tx(fb, C::kTx);
-        bulk_g2s(smem_u32(sm_w + st * kWChunkBytes), p.w + w_chunk_offset(nt, ks, KS),
-                 kWChunkBytes, fb, policy);
-        bulk_g2s(smem_u32(sm_s + st * C::kSBytes),
-                 p.s + static_cast<size_t>(nt * KS + ks) * C::kSBytes, C::kSBytes, fb, policy);
-        const uint32_t a_dst = smem_u32(sm_a + st * C::kABytes);
-        tma_load_2d(a_dst, &tmap_a, static_cast<int32_t>(ks * kStageK),
-                    static_cast<int32_t>(mt * BN), fb);
-        tma_load_2d(a_dst + C::kAHalfBytes, &tmap_a, static_cast<int32_t>(ks * kStageK + 64),
-                    static_cast<int32_t>(mt * BN), fb);
+        bulk_g2s(smem_u32(sm_w + st * C::kWBytes),
+                 p.rep + chunk_offset<FMT>(nt, ku * KU, KS * KU), C::kWBytes, fb, policy);
+        tma_load_3d(smem_u32(sm_a + st * C::kABytes), &tmap_a, 0, static_cast<int32_t>(mt * BN),
+                    static_cast<int32_t>(ku * 2 * KU), fb);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
@@ -197,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t u = u0; u < u1; ++u, ++i) {
         const int st = static_cast<int>(i % C::kStages);
         const uint32_t ph = static_cast<uint32_t>((i / C::kStages) & 1);
-        const int b = static_cast<int>(i % kNumABufs);
-        const uint32_t pb = static_cast<uint32_t>((i / kNumABufs) & 1);
+        const int b = static_cast<int>(i % C::kNumA);
+        const uint32_t pb = static_cast<uint32_t>((i / C::kNumA) & 1);
         const bool first = (u == u0) || (u % KS == 0);
         const bool last = (u == u1 - 1) || (u % KS == KS - 1);
         const int d = static_cast<int>(seg % C::kNumD);
@@ -207,13 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&afull[b], pb)) break;
         tc_fence_after();
         const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
-        const uint32_t d_tmem = tmem + kDColBase + d * BN;
+        const uint32_t d_tmem = tmem + C::kDColBase + d * BN;
+        const uint32_t a_tmem = tmem + b * C::kAColsPerUnit;
 #pragma unroll
-        for (int j = 0; j < kStageK / 16; ++j) {
+        for (int j = 0; j < KU * (kStageK / 16); ++j) {
+          // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
           const uint64_t bdesc =
               smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) + (((j & 3) * 32) >> 4);
-          mma_ts_f16(d_tmem, tmem + b * kAColsPerBuf + j * 8, bdesc, C::kIdesc,
-                     (first && j == 0) ? 0u : 1u);
+          mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc, (first && j == 0) ? 0u : 1u);
         }
         mma_commit(smem_u32(&empty[st]));
         mma_commit(smem_u32(&aempty[b]));
@@ -251,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int d = static_cast<int>(seg % C::kNumD);
       if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDColBase + d * BN;
+      const uint32_t tbase =
+          tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
       const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
       const int64_t slot = 2 * cta + (tile == first_tile_of_cta ? 0 : 1);
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
@@ -290,17 +293,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!epi_sync()) break;
         if (*epi_flag) {
           __threadfence();
+          // contributors' partials are summed in CTA order (deterministic);
+          // loads are batched (up to 4 contributors x 16 columns in flight)
+          // so the reduction costs a few L2 round trips, not one per value
 #pragma unroll 1
-          for (int col = 0; col < BN; ++col) {
-            const int64_t mrow = static_cast<int64_t>(mt) * BN + col;
-            if (mrow >= p.m) break;
-            float acc = 0.0f;
-            for (int64_t c = c_first; c <= c_last; ++c) {
-              const int64_t cs = 2 * c + ((c * U / P) / KS == tile ? 0 : 1);
-              acc += ld_cg_f32(p.partials + static_cast<size_t>(cs) * (BN * kTileN) +
-                               col * kTileN + r);
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+            for (int64_t cb = c_first; cb <= c_last; cb += 4) {
+              float t[4][16];
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const int64_t c = cb + x;
+                if (c <= c_last) {
+                  const int64_t cs = 2 * c + ((c * U / P) / KS == tile ? 0 : 1);
+                  const float* src =
+                      p.partials + static_cast<size_t>(cs) * (BN * kTileN) + c0 * kTileN + r;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) t[x][j] = __ldcg(src + j * kTileN);
+                }
+              }
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                if (cb + x <= c_last) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
+                }
+              }
             }
-            p.c[mrow * p.n + ncol] = __float2bfloat16_rn(p.alpha * acc);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
+              if (mrow < p.m) p.c[mrow * p.n + ncol] = __float2bfloat16_rn(p.alpha * acc[j]);
+            }
           }
         }
         if (!epi_sync()) break;
@@ -310,45 +337,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- dequantise
     const int dw = warp - kDeqWarp0;
-    const int h = dw >> 2;          // which 64-k half of the stage
+    const int h = dw >> 2;          // which 64-k half of each chunk
     const int q = warp & 3;         // tensor-memory lane quarter
     const int r = 32 * q + lane;    // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // Two-deep software pipeline: the tensor-memory stores of unit i-1 are
+    // drained (wait::st) only after unit i has been loaded and decoded, so
+    // their latency overlaps useful work.
+    int prev_b = -1;
     int64_t i = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
       const int st = static_cast<int>(i % C::kStages);
       const uint32_t ph = static_cast<uint32_t>((i / C::kStages) & 1);
-      const int b = static_cast<int>(i % kNumABufs);
-      const uint32_t pb = static_cast<uint32_t>((i / kNumABufs) & 1);
+      const int b = static_cast<int>(i % C::kNumA);
+      const uint32_t pb = static_cast<uint32_t>((i / C::kNumA) & 1);
       if (!wait(&full[st], ph)) break;
       if (!wait(&aempty[b], pb ^ 1u)) break;
-      const uint8_t* wsm = sm_w + st * kWChunkBytes;
-      const uint4 g0 = *reinterpret_cast<const uint4*>(wsm + ((2 * h) * kTileN + r) * 16);
-      const uint4 g1 = *reinterpret_cast<const uint4*>(wsm + ((2 * h + 1) * kTileN + r) * 16);
-      uint32_t sc0, sc1;
-      if constexpr (FMT == kNVFP4) {
-        const uint32_t v =
-            *reinterpret_cast<const uint32_t*>(sm_s + st * C::kSBytes + (h * kTileN + r) * 4);
-        sc0 = v & 0xFFFFu;
-        sc1 = v >> 16;
-      } else {
-        const uint32_t v =
-            *reinterpret_cast<const uint16_t*>(sm_s + st * C::kSBytes + (h * kTileN + r) * 2);
-        sc0 = v & 0xFFu;
-        sc1 = v >> 8;
+      uint4 g[KU][2];
+      uint32_t sv[KU];
+#pragma unroll
+      for (int j = 0; j < KU; ++j) {
+        const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+        g[j][0] = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+        g[j][1] = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+        if constexpr (FMT == kNVFP4)
+          sv[j] = *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
+        else
+          sv[j] = *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-      uint32_t o0[16], o1[16];
-      decode_group<FMT>(g0, sc0, o0);
-      decode_group<FMT>(g1, sc1, o1);
-      const uint32_t acol = tmem + lane_base + b * kAColsPerBuf + (2 * h) * 16;
-      tmem_st_x16(acol, o0);
-      tmem_st_x16(acol + 16, o1);
+      uint32_t o[KU][2][16];
+#pragma unroll
+      for (int j = 0; j < KU; ++j) {
+        if constexpr (FMT == kNVFP4) {
+          decode_group<FMT>(g[j][0], sv[j] & 0xFFFFu, o[j][0]);
+          decode_group<FMT>(g[j][1], sv[j] >> 16, o[j][1]);
+        } else {
+          decode_group<FMT>(g[j][0], sv[j] & 0xFFu, o[j][0]);
+          decode_group<FMT>(g[j][1], (sv[j] >> 8) & 0xFFu, o[j][1]);
+        }
+      }
+      if (prev_b >= 0) {
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull[prev_b]));
+      }
+#pragma unroll
+      for (int j = 0; j < KU; ++j) {
+        const uint32_t acol =
+            tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+        tmem_st_x16(acol, o[j][0]);
+        tmem_st_x16(acol + 16, o[j][1]);
+      }
+      prev_b = b;
+    }
+    if (prev_b >= 0) {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
+      if (lane == 0 && !*abort_flag) mbar_arrive(smem_u32(&afull[prev_b]));
     }
   }
 
@@ -358,16 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int FMT, int BN>
+template <int FMT, int BN, int KU>
 cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t stream) {
-  using C = Cfg<FMT, BN>;
+  using C = Cfg<FMT, BN, KU>;
   static int attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, KU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
@@ -376,16 +425,24 @@ cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t st
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN>, prm, tmap);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN, KU>, prm, tmap);
 }
 
 template <int FMT>
-cudaError_t launch_fmt(int bn, const Params& prm, const CUtensorMap& tmap, cudaStream_t s) {
+cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tmap, cudaStream_t s) {
+  if (ku == 2) {
+    switch (bn) {
+      case 16: return launch_t<FMT, 16, 2>(prm, tmap, s);
+      case 32: return launch_t<FMT, 32, 2>(prm, tmap, s);
+      case 64: return launch_t<FMT, 64, 2>(prm, tmap, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 16: return launch_t<FMT, 16>(prm, tmap, s);
-    case 32: return launch_t<FMT, 32>(prm, tmap, s);
-    case 64: return launch_t<FMT, 64>(prm, tmap, s);
-    case 128: return launch_t<FMT, 128>(prm, tmap, s);
+    case 16: return launch_t<FMT, 16, 1>(prm, tmap, s);
+    case 32: return launch_t<FMT, 32, 1>(prm, tmap, s);
+    case 64: return launch_t<FMT, 64, 1>(prm, tmap, s);
+    case 128: return launch_t<FMT, 128, 1>(prm, tmap, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -398,15 +455,17 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
   GemmPlan pl{};
   pl.fmt = fmt;
   pl.bn = m <= 16 ? 16 : (m <= 32 ? 32 : (m <= 64 ? 64 : 128));
+  // two chunks per unit halves the copy requests when the A tile is small
+  pl.ku = (pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
   pl.m_tiles = static_cast<int>((m + pl.bn - 1) / pl.bn);
   pl.n_tiles = static_cast<int>(n / kTileN);
   pl.k_stages = static_cast<int>(k / kStageK);
-  pl.units = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles * pl.k_stages;
+  pl.units = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles * (pl.k_stages / pl.ku);
   pl.num_ctas = static_cast<int>(pl.units < num_sms ? pl.units : num_sms);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
   pl.ws.counters_off = kWsHeaderBytes;
-  pl.ws.partials_off =
-      align_up(pl.ws.counters_off + sizeof(uint32_t) * static_cast<size_t>(pl.n_tiles) * pl.m_tiles, 256);
+  pl.ws.partials_off = align_up(
+      pl.ws.counters_off + sizeof(uint32_t) * static_cast<size_t>(pl.n_tiles) * pl.m_tiles, 256);
   pl.ws.total = pl.ws.partials_off +
                 sizeof(float) * 2ull * static_cast<size_t>(pl.num_ctas) * pl.bn * kTileN;
   return pl;
@@ -415,8 +474,7 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
 cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap& tmap,
                         cudaStream_t stream) {
   Params prm{};
-  prm.w = a.w;
-  prm.s = a.s;
+  prm.rep = a.rep;
   prm.c = static_cast<__nv_bfloat16*>(a.C);
   prm.partials = reinterpret_cast<float*>(a.workspace + pl.ws.partials_off);
   prm.counters = reinterpret_cast<uint32_t*>(a.workspace + pl.ws.counters_off);
@@ -424,13 +482,13 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   prm.m = static_cast<int32_t>(a.m);
   prm.n = static_cast<int32_t>(a.n);
   prm.m_tiles = pl.m_tiles;
-  prm.k_stages = pl.k_stages;
+  prm.k_units = pl.k_stages / pl.ku;
   prm.units = pl.units;
   prm.num_ctas = pl.num_ctas;
   prm.alpha = a.alpha;
   prm.timeout_ns = a.timeout_ns;
-  if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, prm, tmap, stream);
-  return launch_fmt<kMXFP4>(pl.bn, prm, tmap, stream);
+  if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream);
+  return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream);
 }
 
 }  // namespace petit

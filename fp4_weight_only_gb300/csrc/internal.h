@@ -23,10 +23,11 @@ struct WsLayout {
 struct GemmPlan {
   int fmt;
   int bn;          // activation rows per tile (MMA N)
+  int ku;          // 128-k chunks per pipeline unit (1 or 2)
   int m_tiles;
   int n_tiles;
-  int k_stages;
-  int64_t units;   // n_tiles * m_tiles * k_stages
+  int k_stages;    // 128-k chunks per tile row
+  int64_t units;   // n_tiles * m_tiles * k_stages / ku
   int num_ctas;
   WsLayout ws;
 };
@@ -35,8 +36,7 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
 
 struct GemmArgs {
   const void* A;
-  const uint8_t* w;
-  const uint8_t* s;
+  const uint8_t* rep;   // repacked codes + scales
   void* C;
   int64_t m, n, k;
   float alpha;
@@ -50,10 +50,10 @@ cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, const CUtens
 cudaError_t launch_absmax(const void* x, int64_t count, float* out, cudaStream_t stream);
 cudaError_t launch_quantize(int fmt, const void* W, float g, uint8_t* wp, uint8_t* sp,
                             int64_t n, int64_t k, cudaStream_t stream);
-cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* wo,
-                          uint8_t* so, int64_t n, int64_t k, cudaStream_t stream);
-cudaError_t launch_dequant(int fmt, const uint8_t* wr, const uint8_t* sr, void* out,
-                           int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* out,
+                          int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_dequant(int fmt, const uint8_t* rep, void* out, int64_t n, int64_t k,
+                           cudaStream_t stream);
 cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace petit

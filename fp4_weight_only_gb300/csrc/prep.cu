@@ -145,12 +145,12 @@ __global__ void quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ W,
 // ------------------------------------------------------------------- repack
 // One CTA per (stage, tile) chunk: 128 rows x 64 bytes of packed codes are
 // staged through shared memory so both the reads and the writes are
-// contiguous; each 32-bit word's 8 codes are moved to their decode positions.
+// contiguous; each 32-bit word's 8 codes are moved to their decode positions,
+// and the chunk's scale bytes are appended after its codes.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restrict__ wp,
                                                           const uint8_t* __restrict__ sp,
-                                                          uint8_t* __restrict__ wo,
-                                                          uint8_t* __restrict__ so, int64_t k) {
+                                                          uint8_t* __restrict__ out, int64_t k) {
   using T = FmtTraits<FMT>;
   const int64_t stages = k / kStageK;
   const int64_t s = blockIdx.x;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
                                                  s * (kStageK / 2) + g * 16);
   }
   __syncthreads();
-  uint8_t* dst = wo + w_chunk_offset(t, s, stages);
+  uint8_t* dst = out + chunk_offset<FMT>(t, s, stages);
   for (int i = threadIdx.x; i < kTileN * kGroupsPerRow; i += kThreads) {
     const int g = i >> 7, r = i & 127;
     const uint4 in = tile[r][g];
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
   // scales: half h of row r <- bytes [h * B, h * B + B) of the stage's bytes
   constexpr int B = T::kScaleBytesPerHalf;
   const int64_t srow_bytes = k / T::kBlock;
-  uint8_t* sdst = so + static_cast<size_t>((t * stages + s) * T::kSChunkBytes);
+  uint8_t* sdst = dst + kWChunkBytes;
   for (int i = threadIdx.x; i < 2 * kTileN; i += kThreads) {
     const int h = i >> 7, r = i & 127;
     const uint8_t* src = sp + (t * kTileN + r) * srow_bytes + s * (2 * B) + h * B;
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
 // One thread per (chunk, group, row): decodes 32 codes with the GEMM's decode
 // and writes Wq = code * scale as BF16 [n][k].
 template <int FMT>
-__global__ void dequant_kernel(const uint8_t* __restrict__ wr, const uint8_t* __restrict__ sr,
-                               __nv_bfloat16* __restrict__ out, int64_t n, int64_t k) {
+__global__ void dequant_kernel(const uint8_t* __restrict__ rep, __nv_bfloat16* __restrict__ out,
+                               int64_t n, int64_t k) {
   using T = FmtTraits<FMT>;
   const int64_t stages = k / kStageK;
   const int64_t total = (n / kTileN) * stages * (kTileN * kGroupsPerRow);
@@ -210,13 +210,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wr, const uint8_t* __
     const int within = static_cast<int>(idx & 511);
     const int g = within >> 7, r = within & 127, h = g >> 1;
     const int64_t t = chunk / stages, s = chunk % stages;
-    const uint4 grp = *reinterpret_cast<const uint4*>(wr + chunk * kWChunkBytes + within * 16);
+    const uint8_t* cbase = rep + chunk * T::kChunkBytes;
+    const uint4 grp = *reinterpret_cast<const uint4*>(cbase + within * 16);
     uint32_t sc;
     if constexpr (FMT == kNVFP4) {
-      sc = *reinterpret_cast<const uint16_t*>(sr + chunk * T::kSChunkBytes + (h * 128 + r) * 4 +
-                                              (g & 1) * 2);
+      sc = *reinterpret_cast<const uint16_t*>(cbase + kWChunkBytes + (h * 128 + r) * 4 + (g & 1) * 2);
     } else {
-      sc = sr[chunk * T::kSChunkBytes + (h * 128 + r) * 2 + (g & 1)];
+      sc = cbase[kWChunkBytes + (h * 128 + r) * 2 + (g & 1)];
     }
     uint32_t o[16];
     decode_group<FMT>(grp, sc, o);
@@ -267,24 +267,24 @@ cudaError_t launch_quantize(int fmt, const void* W, float g, uint8_t* wp, uint8_
   return cudaGetLastError();
 }
 
-cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* wo,
-                          uint8_t* so, int64_t n, int64_t k, cudaStream_t stream) {
+cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t* out,
+                          int64_t n, int64_t k, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(k / kStageK), static_cast<unsigned>(n / kTileN));
   if (fmt == kNVFP4)
-    repack_kernel<kNVFP4><<<grid, kThreads, 0, stream>>>(wp, sp, wo, so, k);
+    repack_kernel<kNVFP4><<<grid, kThreads, 0, stream>>>(wp, sp, out, k);
   else
-    repack_kernel<kMXFP4><<<grid, kThreads, 0, stream>>>(wp, sp, wo, so, k);
+    repack_kernel<kMXFP4><<<grid, kThreads, 0, stream>>>(wp, sp, out, k);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(int fmt, const uint8_t* wr, const uint8_t* sr, void* out, int64_t n,
-                           int64_t k, cudaStream_t stream) {
+cudaError_t launch_dequant(int fmt, const uint8_t* rep, void* out, int64_t n, int64_t k,
+                           cudaStream_t stream) {
   const int64_t total = (n / kTileN) * (k / kStageK) * (kTileN * kGroupsPerRow);
   auto* o = static_cast<__nv_bfloat16*>(out);
   if (fmt == kNVFP4)
-    dequant_kernel<kNVFP4><<<grid_for(total), kThreads, 0, stream>>>(wr, sr, o, n, k);
+    dequant_kernel<kNVFP4><<<grid_for(total), kThreads, 0, stream>>>(rep, o, n, k);
   else
-    dequant_kernel<kMXFP4><<<grid_for(total), kThreads, 0, stream>>>(wr, sr, o, n, k);
+    dequant_kernel<kMXFP4><<<grid_for(total), kThreads, 0, stream>>>(rep, o, n, k);
   return cudaGetLastError();
 }
 

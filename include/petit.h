@@ -20,8 +20,9 @@
  *
  * Weights are used through an offline "repack" (Petit PyPI page, "Techniques
  * and performance": weights are shuffled offline, as in Marlin, so the GPU
- * dequantises cheaply).  The repacked buffers have exactly the byte size of
- * their inputs and an opaque, versioned order (petit_layout_version()).
+ * dequantises cheaply).  The repacked buffer holds the codes and the scales
+ * (exactly the bytes of both inputs) in an opaque, versioned order
+ * (petit_layout_version()).
  *
  * Conventions for every entry point:
  *   - Pointers marked (device) are CUDA device pointers; the caller allocates
@@ -73,11 +74,9 @@ const char* petit_status_string(petit_status_t status);
 
 /* ------------------------------------------------------------------ sizes */
 
-/* Bytes of the repacked weight buffer: n*k/2 (same as the packed input). */
-size_t petit_repacked_weight_bytes(int64_t n, int64_t k);
-
-/* Bytes of the repacked scale buffer: n*k/16 (NVFP4) or n*k/32 (MXFP4). */
-size_t petit_repacked_scale_bytes(int64_t n, int64_t k, int fmt);
+/* Bytes of a repacked weight buffer: n*k/2 code bytes plus n*k/16 (NVFP4) or
+ * n*k/32 (MXFP4) scale bytes; 0 for an unknown format. */
+size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt);
 
 /* Bytes of GEMM workspace for this problem on the current device (holds a
  * device status word, per-tile arrival counters and FP32 split-K partials).
@@ -118,53 +117,53 @@ petit_status_t petit_quantize_mxfp4(const void* W, uint8_t* w_packed,
 
 /* Offline repack (Marlin-style shuffle; Petit blog, "Efficient dequantization
  * via preprocessing"): permutes the packed codes and the scale bytes into the
- * per-tile, per-pipeline-stage order the GEMM streams, with each 32-bit word
- * holding its 8 codes in the bit positions the in-register BF16 decode uses.
- * Inputs w_packed [n][k/2], s_e4m3 [n][k/16] (device, read only); outputs
- * w_out (petit_repacked_weight_bytes), s_out (petit_repacked_scale_bytes)
- * (device, must not overlap the inputs).  n % 128 == 0, k % 128 == 0.
+ * per-tile, per-pipeline-stage order the GEMM streams -- for each 128-row x
+ * 128-k chunk, its codes followed by its scales, so one contiguous copy
+ * brings both -- with each 32-bit word holding its 8 codes in the bit
+ * positions the in-register BF16 decode uses.
+ * Inputs w_packed [n][k/2], s_e4m3 [n][k/16] (device, read only); output
+ * rep_out of petit_repacked_bytes(n, k, PETIT_FMT_NVFP4) bytes (device, must
+ * not overlap the inputs).  n % 128 == 0, k % 128 == 0.
  * Scales must be positive (not 0x00, 0x7F or negative) -- the precondition of
  * Petit's offline transform (Petit PyPI page, "Known limitations"); the
  * library does not check them.  Negative-zero codes are harmless here (they
  * decode to -0.0). */
 petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3,
-                                  uint8_t* w_out, uint8_t* s_out,
-                                  int64_t n, int64_t k, petit_stream_t stream);
+                                  uint8_t* rep_out, int64_t n, int64_t k,
+                                  petit_stream_t stream);
 
 /* Same as petit_repack_nvfp4 for MXFP4 scales s_e8m0 [n][k/32] (code 0xFF is
  * not a number and must not occur). */
 petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0,
-                                  uint8_t* w_out, uint8_t* s_out,
-                                  int64_t n, int64_t k, petit_stream_t stream);
+                                  uint8_t* rep_out, int64_t n, int64_t k,
+                                  petit_stream_t stream);
 
 /* Test hook: dequantise repacked weights with the GEMM's own device decode
  * routine and write Wq = code * block_scale as BF16, row-major [n][k]
  * (device).  The global scale is not applied.  Wq is exactly representable,
  * so the result is bit-exact.  (The per-block dump suggested as a debugging
  * aid in "FP4 GEMM on Rubin/Blackwell with CUTLASS", section 7.) */
-petit_status_t petit_dequant_bf16(const uint8_t* w_rep, const uint8_t* s_rep,
-                                  int fmt, void* W_out, int64_t n, int64_t k,
-                                  petit_stream_t stream);
+petit_status_t petit_dequant_bf16(const uint8_t* rep, int fmt, void* W_out,
+                                  int64_t n, int64_t k, petit_stream_t stream);
 
 /* --------------------------------------------------------------- the GEMM */
 
 /* C[m][n] = bf16(g * sum_k A[m][k] * Wq[n][k]) with FP32 accumulation.
- * A: BF16 [m][k] (device); w_rep / s_rep: repacked NVFP4 weights and E4M3
- * scales (device); C: BF16 [m][n] (device, must not overlap A);
+ * A: BF16 [m][k] (device); rep: repacked NVFP4 weights and E4M3 scales
+ * (device); C: BF16 [m][n] (device, must not overlap A);
  * workspace: at least petit_gemm_workspace_bytes(m, n, k, PETIT_FMT_NVFP4)
  * zero-filled bytes (device).  m >= 1 (any value); n % 128 == 0;
  * k % 128 == 0.  Calls that share a workspace must not run concurrently.
  * Device-side waits are bounded: if one runs out, the kernel stops early,
  * C is not valid, and petit_get_device_status() reports PETIT_ERR_TIMEOUT. */
-petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* w_rep,
-                                     const uint8_t* s_rep, float global_scale,
-                                     void* C, int64_t m, int64_t n, int64_t k,
+petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* rep,
+                                     float global_scale, void* C,
+                                     int64_t m, int64_t n, int64_t k,
                                      void* workspace, size_t workspace_bytes,
                                      petit_stream_t stream);
 
 /* Same with repacked MXFP4 weights and E8M0 scales (no global scale). */
-petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* w_rep,
-                                     const uint8_t* s_rep, void* C,
+petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,
                                      int64_t m, int64_t n, int64_t k,
                                      void* workspace, size_t workspace_bytes,
                                      petit_stream_t stream);

@@ -44,10 +44,9 @@ def test_host_only_entry_points(lib):
     for s in range(8):
         assert lib.petit_status_string(s)
     assert lib.petit_status_string(99) == b"unknown status"
-    assert lib.petit_repacked_weight_bytes(8192, 8192) == 8192 * 4096
-    assert lib.petit_repacked_scale_bytes(8192, 8192, 0) == 8192 * 512
-    assert lib.petit_repacked_scale_bytes(8192, 8192, 1) == 8192 * 256
-    assert lib.petit_repacked_scale_bytes(8192, 8192, 7) == 0
+    assert lib.petit_repacked_bytes(8192, 8192, 0) == 8192 * 4096 + 8192 * 512
+    assert lib.petit_repacked_bytes(8192, 8192, 1) == 8192 * 4096 + 8192 * 256
+    assert lib.petit_repacked_bytes(8192, 8192, 7) == 0
     assert lib.petit_nvfp4_global_scale(ctypes.c_float(2688.0)) == 1.0
 
 
@@ -60,19 +59,19 @@ def test_argument_validation_without_gpu(lib):
     NULL = P(0)
     s = P(0)
     # null pointer / m < 1
-    assert lib.petit_gemm_bf16_nvfp4(NULL, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
-    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 0, 1024, 1024, a, 1 << 20, s) == 1
-    assert lib.petit_gemm_bf16_nvfp4(a, a, a, -1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
+    assert lib.petit_gemm_bf16_nvfp4(NULL, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
+    assert lib.petit_gemm_bf16_nvfp4(a, a, 1.0, a, 0, 1024, 1024, a, 1 << 20, s) == 1
+    assert lib.petit_gemm_bf16_nvfp4(a, a, -1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 1
     # shapes: n, k multiples of 128
-    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 16, 1000, 1024, a, 1 << 20, s) == 2
-    assert lib.petit_gemm_bf16_mxfp4(a, a, a, a, 16, 1024, 1056, a, 1 << 20, s) == 2
+    assert lib.petit_gemm_bf16_nvfp4(a, a, 1.0, a, 16, 1000, 1024, a, 1 << 20, s) == 2
+    assert lib.petit_gemm_bf16_mxfp4(a, a, a, 16, 1024, 1056, a, 1 << 20, s) == 2
     # alignment
-    assert lib.petit_gemm_bf16_nvfp4(bad, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 3
+    assert lib.petit_gemm_bf16_nvfp4(bad, a, 1.0, a, 16, 1024, 1024, a, 1 << 20, s) == 3
     # workspace missing
-    assert lib.petit_gemm_bf16_mxfp4(a, a, a, a, 16, 1024, 1024, NULL, 0, s) == 4
-    assert lib.petit_repack_nvfp4(a, a, a, a, 100, 1024, s) == 2
-    assert lib.petit_repack_mxfp4(a, NULL, a, a, 128, 128, s) == 1
-    assert lib.petit_dequant_bf16(a, a, 5, a, 128, 128, s) == 1
+    assert lib.petit_gemm_bf16_mxfp4(a, a, a, 16, 1024, 1024, NULL, 0, s) == 4
+    assert lib.petit_repack_nvfp4(a, a, a, 100, 1024, s) == 2
+    assert lib.petit_repack_mxfp4(a, NULL, a, 128, 128, s) == 1
+    assert lib.petit_dequant_bf16(a, 5, a, 128, 128, s) == 1
     assert lib.petit_quantize_nvfp4(a, ctypes.c_float(0.0), a, a, 4, 32, s) == 1
     assert lib.petit_quantize_mxfp4(a, a, a, 4, 48, s) == 2
     assert lib.petit_absmax_bf16(a, 0, a, s) == 1
@@ -90,5 +89,5 @@ def test_no_device_is_reported_not_crashed(lib):
         pytest.skip("a GPU is present")
     a = P(0x10000)
     # valid arguments, but no usable device: a CUDA error status, never a crash
-    assert lib.petit_gemm_bf16_nvfp4(a, a, a, 1.0, a, 16, 1024, 1024, a, 1 << 30, P(0)) == 6
+    assert lib.petit_gemm_bf16_nvfp4(a, a, 1.0, a, 16, 1024, 1024, a, 1 << 30, P(0)) == 6
     assert lib.petit_gemm_workspace_bytes(16, 1024, 1024, 0) == 0

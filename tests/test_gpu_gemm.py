@@ -25,19 +25,18 @@ pytestmark = pytest.mark.gpu
 def _prep(cuda_lib, w, fmt, g=1.0):
     codes, scales = oracle_quantize(w, fmt, g)
     wp, sp = to_device_packed(codes, scales)
-    wr, sr = cuda_lib.repack(wp, sp, fmt)
-    return codes, scales, wr, sr
+    return codes, scales, cuda_lib.repack(wp, sp, fmt)
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
 @pytest.mark.parametrize("m,n,k", [(1024, 1024, 1024), (16, 256, 2048), (200, 384, 640)])
 def test_one_hot_is_bit_exact(cuda_lib, fmt, m, n, k):
     w = synth.weights(n, k, seed=5)
-    codes, scales, wr, sr = _prep(cuda_lib, w, fmt)
+    codes, scales, rep = _prep(cuda_lib, w, fmt)
     rng = np.random.default_rng(m + n + k)
     cols = rng.permutation(k)[:m] if m <= k else rng.integers(0, k, m)
     a = synth.one_hot_activations(m, k, cols).cuda()
-    c = cuda_lib.gemm(a, wr, sr, n, fmt, 1.0)
+    c = cuda_lib.gemm(a, rep, n, fmt, 1.0)
     torch.cuda.synchronize()
     wq_bits = ogemm.dequantize_bf16_bits(codes, scales, fmt)      # [n, k]
     expect = wq_bits[:, cols].T                                   # C[i, :] = Wq[:, cols[i]]
@@ -51,19 +50,31 @@ def test_one_hot_is_bit_exact(cuda_lib, fmt, m, n, k):
 def test_nvfp4_parity_ragged_m(cuda_lib, m):
     n, k = 1024, 1024
     w = synth.weights(n, k, seed=1)
-    codes, scales, wr, sr = _prep(cuda_lib, w, "nvfp4")
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     a = synth.activations(m, k, seed=m)
-    c = cuda_lib.gemm(a.cuda(), wr, sr, n, "nvfp4", 1.0)
+    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", 1.0)
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), f"m={m}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("m", [4, 40, 130])
+def test_odd_chunk_count(cuda_lib, fmt, m):
+    """k = 9 x 128: pipeline units of a single 128-k chunk at every m."""
+    n, k = 256, 1152
+    w = synth.weights(n, k, seed=12)
+    codes, scales, rep = _prep(cuda_lib, w, fmt)
+    a = synth.activations(m, k, seed=13)
+    c = cuda_lib.gemm(a.cuda(), rep, n, fmt, 1.0)
+    assert_parity(c, oracle_reference(a, codes, scales, fmt), f"m={m}")
 
 
 @pytest.mark.parametrize("m", [1, 4, 8, 16, 100])
 def test_mxfp4_parity(cuda_lib, m):
     n, k = 768, 2048
     w = synth.weights(n, k, seed=2)
-    codes, scales, wr, sr = _prep(cuda_lib, w, "mxfp4")
+    codes, scales, rep = _prep(cuda_lib, w, "mxfp4")
     a = synth.activations(m, k, seed=10 + m)
-    c = cuda_lib.gemm(a.cuda(), wr, sr, n, "mxfp4")
+    c = cuda_lib.gemm(a.cuda(), rep, n, "mxfp4")
     assert_parity(c, oracle_reference(a, codes, scales, "mxfp4"), f"m={m}")
 
 
@@ -73,40 +84,40 @@ def test_nvfp4_global_scale_and_outliers(cuda_lib, m):
     n, k = 640, 1536
     w = synth.weights(n, k, seed=3)
     g = float(quantize.nvfp4_global_scale(w.float().numpy()))
-    codes, scales, wr, sr = _prep(cuda_lib, w, "nvfp4", g)
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4", g)
     a = synth.activations(m, k, seed=4, outlier_frac=0.001, outlier_std=20.0)
-    c = cuda_lib.gemm(a.cuda(), wr, sr, n, "nvfp4", g)
+    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", g)
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4", g), f"m={m}")
 
 
 def test_special_cases(cuda_lib):
     n, k = 256, 512
     w = synth.weights(n, k, seed=6)
-    codes, scales, wr, sr = _prep(cuda_lib, w, "nvfp4")
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     z = torch.zeros((7, k), dtype=torch.bfloat16, device="cuda")
-    c = cuda_lib.gemm(z, wr, sr, n, "nvfp4")
+    c = cuda_lib.gemm(z, rep, n, "nvfp4")
     assert torch.all(c == 0)
     # all-zero weights (zero codes, smallest positive scale)
     zw = torch.zeros((n, k), dtype=torch.bfloat16)
-    codes0, scales0, wr0, sr0 = _prep(cuda_lib, zw, "nvfp4")
+    codes0, scales0, rep0 = _prep(cuda_lib, zw, "nvfp4")
     assert np.all(codes0 == 0)
     a = synth.activations(9, k, seed=7).cuda()
-    assert torch.all(cuda_lib.gemm(a, wr0, sr0, n, "nvfp4") == 0)
+    assert torch.all(cuda_lib.gemm(a, rep0, n, "nvfp4") == 0)
     # all-ones activations give (BF16-rounded) row sums
     ones = torch.ones((1, k), dtype=torch.bfloat16, device="cuda")
-    assert_parity(cuda_lib.gemm(ones, wr, sr, n, "nvfp4"),
+    assert_parity(cuda_lib.gemm(ones, rep, n, "nvfp4"),
                   oracle_reference(ones.cpu(), codes, scales, "nvfp4"), "ones")
 
 
 def test_deterministic_and_workspace_reuse(cuda_lib):
     n, k = 1024, 2048
     w = synth.weights(n, k, seed=8)
-    codes, scales, wr, sr = _prep(cuda_lib, w, "nvfp4")
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     ws = cuda_lib.Workspace()
     outs = []
     for m in (16, 100, 16, 3, 16):
         a = synth.activations(m, k, seed=21).cuda()
-        outs.append((m, cuda_lib.gemm(a, wr, sr, n, "nvfp4", 1.0, workspace=ws).clone()))
+        outs.append((m, cuda_lib.gemm(a, rep, n, "nvfp4", 1.0, workspace=ws).clone()))
     assert ws.status() == 0
     c16 = [c for m, c in outs if m == 16]
     assert all(torch.equal(c16[0], c) for c in c16[1:])
@@ -127,8 +138,8 @@ def test_bounded_wait_reports_timeout(cuda_lib):
     assert ws.status() == 0                      # cleared by the read
     n, k = 256, 256
     w = synth.weights(n, k, seed=9)
-    codes, scales, wr, sr = _prep(cuda_lib, w, "nvfp4")
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     a = synth.activations(4, k, seed=9)
-    c = cuda_lib.gemm(a.cuda(), wr, sr, n, "nvfp4", workspace=ws)
+    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", workspace=ws)
     assert ws.status() == 0
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), "after timeout")

@@ -47,11 +47,18 @@ def test_repack_dequant_bitexact(cuda_lib, fmt, n, k):
     # also exercise every code value, including negative zero (decodes to -0.0)
     codes[5, :16] = np.arange(16)
     wp, sp = to_device_packed(codes, scales)
-    wr, sr = cuda_lib.repack(wp, sp, fmt)
-    assert wr.numel() == n * k // 2 and sr.numel() == scales.size
-    # the repack is a permutation: byte and nibble histograms are kept
-    assert sorted(sr.cpu().numpy().tolist()) == sorted(scales.reshape(-1).tolist())
-    out = cuda_lib.dequant(wr, sr, n, k, fmt)
+    rep = cuda_lib.repack(wp, sp, fmt)
+    assert rep.numel() == n * k // 2 + scales.size
+    # the repack permutes bits inside 32-bit code words and moves scale bytes:
+    # the number of set bits and the multiset of scale bytes are kept
+    r = rep.cpu().numpy()
+    packed = quantize.pack_codes(codes)
+    popcount = lambda x: int(np.unpackbits(np.ascontiguousarray(x).view(np.uint8)).sum())
+    assert popcount(r) == popcount(packed) + popcount(scales)
+    chunk = 8192 + (1024 if fmt == "nvfp4" else 512)
+    scale_part = r.reshape(-1, chunk)[:, 8192:]
+    assert sorted(scale_part.reshape(-1).tolist()) == sorted(scales.reshape(-1).tolist())
+    out = cuda_lib.dequant(rep, n, k, fmt)
     torch.cuda.synchronize()
     expect = gemm.dequantize_bf16_bits(codes, scales, fmt)
     got = bf16_bits(out)
@@ -67,8 +74,8 @@ def test_dequant_all_e4m3_scales(cuda_lib):
     scales = np.tile(np.arange(1, 127, dtype=np.uint8), (n * k // 16) // 126 + 1)[: n * k // 16]
     scales = scales.reshape(n, k // 16)
     wp, sp = to_device_packed(codes, scales)
-    wr, sr = cuda_lib.repack(wp, sp, "nvfp4")
-    got = bf16_bits(cuda_lib.dequant(wr, sr, n, k, "nvfp4"))
+    rep = cuda_lib.repack(wp, sp, "nvfp4")
+    got = bf16_bits(cuda_lib.dequant(rep, n, k, "nvfp4"))
     np.testing.assert_array_equal(got, gemm.dequantize_bf16_bits(codes, scales, "nvfp4"))
 
 
@@ -79,6 +86,6 @@ def test_dequant_mx_scale_range(cuda_lib):
     codes = rng.integers(0, 16, (n, k)).astype(np.uint8)
     scales = rng.integers(7, 248, (n, k // 32)).astype(np.uint8)
     wp, sp = to_device_packed(codes, scales)
-    wr, sr = cuda_lib.repack(wp, sp, "mxfp4")
-    got = bf16_bits(cuda_lib.dequant(wr, sr, n, k, "mxfp4"))
+    rep = cuda_lib.repack(wp, sp, "mxfp4")
+    got = bf16_bits(cuda_lib.dequant(rep, n, k, "mxfp4"))
     np.testing.assert_array_equal(got, gemm.dequantize_bf16_bits(codes, scales, "mxfp4"))
