@@ -104,11 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][BN][128 B]
   uint8_t* sm_w = sm_a + C::kStages * C::kABytes;          // [stage][KU chunks]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kStages * C::kWBytes);
+  // full[s]: the stage's copies landed.  mdone[s]: the MMAs of the unit in
+  // stage s completed -- which also means the dequantisers are done reading
+  // it (the MMAs only start after their tensor-memory stores), so one commit
+  // per unit frees both the stage and the unit's tensor-memory A-buffer.
   uint64_t* full = bars;
-  uint64_t* empty = full + C::kStages;
-  uint64_t* afull = empty + C::kStages;
-  uint64_t* aempty = afull + C::kNumA;
-  uint64_t* dfull = aempty + C::kNumA;
+  uint64_t* mdone = full + C::kStages;
+  uint64_t* afull = mdone + C::kStages;
+  uint64_t* dfull = afull + C::kNumA;
   uint64_t* dempty = dfull + C::kNumD;
   uint64_t* fin = dempty + C::kNumD;
   uint64_t* epi_bar = fin + 1;
@@ -128,12 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kNumDeqWarps + 1);
+      mbar_init(smem_u32(&mdone[i]), 1);
     }
-    for (int i = 0; i < C::kNumA; ++i) {
-      mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
-      mbar_init(smem_u32(&aempty[i]), 1);
-    }
+    for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
     for (int i = 0; i < C::kNumD; ++i) {
       mbar_init(smem_u32(&dfull[i]), 1);
       mbar_init(smem_u32(&dempty[i]), 4);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t u = u0; u < u1; ++u, ++issued) {
         const int st = static_cast<int>(issued % C::kStages);
         const uint32_t ph = static_cast<uint32_t>((issued / C::kStages) & 1);
-        if (!wait(&empty[st], ph ^ 1u)) break;
+        if (!wait(&mdone[st], ph ^ 1u)) break;
         const int64_t tile = u / KS, ku = u % KS;
         const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
         const uint32_t fb = smem_u32(&full[st]);
@@ -217,8 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) + (((j & 3) * 32) >> 4);
           mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc, (first && j == 0) ? 0u : 1u);
         }
-        mma_commit(smem_u32(&empty[st]));
-        mma_commit(smem_u32(&aempty[b]));
+        mma_commit(smem_u32(&mdone[st]));
         if (last) {
           mma_commit(smem_u32(&dfull[d]));
           ++seg;
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*epi_flag) {
           __threadfence();
           // contributors' partials are summed in CTA order (deterministic);
-          // loads are batched (up to 4 contributors x 16 columns in flight)
+          // loads are batched (up to 2 contributors x 16 columns in flight)
           // so the reduction costs a few L2 round trips, not one per value
 #pragma unroll 1
           for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -302,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll 1
-            for (int64_t cb = c_first; cb <= c_last; cb += 4) {
-              float t[4][16];
+            for (int64_t cb = c_first; cb <= c_last; cb += 2) {
+              float t[2][16];
 #pragma unroll
-              for (int x = 0; x < 4; ++x) {
+              for (int x = 0; x < 2; ++x) {
                 const int64_t c = cb + x;
                 if (c <= c_last) {
                   const int64_t cs = 2 * c + ((c * U / P) / KS == tile ? 0 : 1);
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
 #pragma unroll
-              for (int x = 0; x < 4; ++x) {
+              for (int x = 0; x < 2; ++x) {
                 if (cb + x <= c_last) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
@@ -350,9 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = static_cast<int>(i % C::kStages);
       const uint32_t ph = static_cast<uint32_t>((i / C::kStages) & 1);
       const int b = static_cast<int>(i % C::kNumA);
-      const uint32_t pb = static_cast<uint32_t>((i / C::kNumA) & 1);
       if (!wait(&full[st], ph)) break;
-      if (!wait(&aempty[b], pb ^ 1u)) break;
+      if (i >= C::kNumA) {
+        // A-buffer b was last used by unit i - kNumA: wait for its MMAs
+        const int64_t j = i - C::kNumA;
+        if (!wait(&mdone[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1))) break;
+      }
       uint4 g[KU][2];
       uint32_t sv[KU];
 #pragma unroll
@@ -365,8 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           sv[j] = *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
       uint32_t o[KU][2][16];
 #pragma unroll
       for (int j = 0; j < KU; ++j) {
