@@ -74,7 +74,7 @@ struct Cfg {
   static constexpr int kStages0 = (212 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   static constexpr int kTx = kStageBytes;
-  static constexpr int kNumD = 2;                              // accumulator buffers
+  static constexpr int kNumD = 2;                              // accumulator buffers (seg & 1)
   static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
   static constexpr int kNumA0 = (static_cast<int>(kTmemCols) - kNumD * BN) / kAColsPerUnit;
   static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
@@ -168,19 +168,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
+      // all per-unit indices advance incrementally: a runtime 64-bit division
+      // costs hundreds of cycles in a single thread
       int64_t issued = 0;
+      int st = 0;
+      uint32_t ph = 0;
+      const int64_t tile0 = u0 / KS;
+      int64_t ku = u0 - tile0 * KS;
+      int64_t nt = tile0 / p.m_tiles;
+      int64_t mt = tile0 - nt * p.m_tiles;
       for (int64_t u = u0; u < u1; ++u, ++issued) {
-        const int st = static_cast<int>(issued % C::kStages);
-        const uint32_t ph = static_cast<uint32_t>((issued / C::kStages) & 1);
         if (!wait(&mdone[st], ph ^ 1u)) break;
-        const int64_t tile = u / KS, ku = u % KS;
-        const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
         const uint32_t fb = smem_u32(&full[st]);
         mbar_arrive_expect_tx(fb, C::kTx);
         bulk_g2s(smem_u32(sm_w + st * C::kWBytes),
                  p.rep + chunk_offset<FMT>(nt, ku * KU, KS * KU), C::kWBytes, fb, policy);
         tma_load_3d(smem_u32(sm_a + st * C::kABytes), &tmap_a, 0, static_cast<int32_t>(mt * BN),
                     static_cast<int32_t>(ku * 2 * KU), fb);
+        if (++st == C::kStages) {
+          st = 0;
+          ph ^= 1u;
+        }
+        if (++ku == KS) {
+          ku = 0;
+          if (++mt == p.m_tiles) {
+            mt = 0;
+            ++nt;
+          }
+        }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
@@ -193,17 +208,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      int64_t i = 0;
       int64_t seg = 0;
-      for (int64_t u = u0; u < u1; ++u, ++i) {
-        const int st = static_cast<int>(i % C::kStages);
-        const uint32_t ph = static_cast<uint32_t>((i / C::kStages) & 1);
-        const int b = static_cast<int>(i % C::kNumA);
-        const uint32_t pb = static_cast<uint32_t>((i / C::kNumA) & 1);
-        const bool first = (u == u0) || (u % KS == 0);
-        const bool last = (u == u1 - 1) || (u % KS == KS - 1);
-        const int d = static_cast<int>(seg % C::kNumD);
-        if (first && !wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
+      int st = 0, b = 0;
+      uint32_t ph = 0, pb = 0;
+      int64_t ku = u0 - (u0 / KS) * KS;
+      for (int64_t u = u0; u < u1; ++u) {
+        const bool first = (u == u0) || (ku == 0);
+        const bool last = (u == u1 - 1) || (ku == KS - 1);
+        const int d = static_cast<int>(seg & 1);
+        if (first && !wait(&dempty[d], static_cast<uint32_t>(((seg >> 1) & 1) ^ 1))) break;
         if (!wait(&full[st], ph)) break;
         if (!wait(&afull[b], pb)) break;
         tc_fence_after();
@@ -222,6 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(smem_u32(&dfull[d]));
           ++seg;
         }
+        if (++st == C::kStages) {
+          st = 0;
+          ph ^= 1u;
+        }
+        if (++b == C::kNumA) {
+          b = 0;
+          pb ^= 1u;
+        }
+        if (++ku == KS) ku = 0;
       }
       // all issued MMAs complete before tensor memory is released
       mma_commit(smem_u32(fin));
@@ -249,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t seg_end = (tile + 1) * KS < u1 ? (tile + 1) * KS : u1;
       const bool full_tile = (u == tile * KS) && (seg_end == (tile + 1) * KS);
       const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
-      const int d = static_cast<int>(seg % C::kNumD);
-      if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
+      const int d = static_cast<int>(seg & 1);
+      if (!wait(&dfull[d], static_cast<uint32_t>((seg >> 1) & 1))) break;
       tc_fence_after();
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
@@ -281,6 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stream-K fix-up: the last contributor sums all partials in CTA order
         const int64_t c_first = cta_of_unit(tile * KS, U, P);
         const int64_t c_last = cta_of_unit((tile + 1) * KS - 1, U, P);
+        // every contributor but the first starts inside this tile (slot 2c);
+        // the first uses its second slot unless its range starts at the tile
+        const int64_t first_slot = 2 * c_first + ((c_first * U / P) / KS == tile ? 0 : 1);
         __threadfence();
         if (!epi_sync()) break;
         if (epi_tid == 0) {
@@ -307,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int x = 0; x < 2; ++x) {
                 const int64_t c = cb + x;
                 if (c <= c_last) {
-                  const int64_t cs = 2 * c + ((c * U / P) / KS == tile ? 0 : 1);
+                  const int64_t cs = c == c_first ? first_slot : 2 * c;
                   const float* src =
                       p.partials + static_cast<size_t>(cs) * (BN * kTileN) + c0 * kTileN + r;
 #pragma unroll
@@ -345,15 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // their latency overlaps useful work.
     int prev_b = -1;
     int64_t i = 0;
+    int st = 0, b = 0, st2 = 0;   // st2: stage of unit i - kNumA
+    uint32_t ph = 0, ph2 = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
-      const int st = static_cast<int>(i % C::kStages);
-      const uint32_t ph = static_cast<uint32_t>((i / C::kStages) & 1);
-      const int b = static_cast<int>(i % C::kNumA);
       if (!wait(&full[st], ph)) break;
       if (i >= C::kNumA) {
         // A-buffer b was last used by unit i - kNumA: wait for its MMAs
-        const int64_t j = i - C::kNumA;
-        if (!wait(&mdone[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1))) break;
+        if (!wait(&mdone[st2], ph2)) break;
+        if (++st2 == C::kStages) {
+          st2 = 0;
+          ph2 ^= 1u;
+        }
       }
       uint4 g[KU][2];
       uint32_t sv[KU];
@@ -392,6 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x16(acol + 16, o[j][1]);
       }
       prev_b = b;
+      if (++st == C::kStages) {
+        st = 0;
+        ph ^= 1u;
+      }
+      if (++b == C::kNumA) b = 0;
     }
     if (prev_b >= 0) {
       tmem_wait_st();
