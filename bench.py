@@ -89,7 +89,7 @@ def ncu_traffic(kernel_file):
                 key, val = line.strip()[1:].split(":", 1)
                 fields[key.strip()] = val.strip()
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if fields.get("gemm.cu sha256[:16]") != digest:
+    if fields.get("gemm.cu sha256 prefix") != digest:
         return None
     try:
         return float(fields["dram bytes per launch (gate_up, scaled)"])
