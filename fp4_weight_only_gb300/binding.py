@@ -53,6 +53,8 @@ SIGNATURES = {
                                              _c_p, _c_sz, _c_p]),
     "petit_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_sz,
                                              _c_p]),
+    "petit_gemm_bf16_nvfp4_noalloc": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
+                                                     _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
 }

@@ -260,3 +260,70 @@ petit_status_t petit_selftest_timeout(void* workspace, size_t workspace_bytes, u
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// GEMM without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they call the GEMM: code
+// running while a CUDA graph is being captured (cudaMalloc is not a stream
+// operation), plug-ins whose host framework owns all device memory and
+// forbids allocation inside their enqueue call, and latency-critical serving
+// loops where cudaMalloc's implicit device synchronisation is unacceptable.
+// For them the split-K scratch (status word, arrival counters, FP32 partial
+// sums) lives in a fixed array in this library's device image instead of a
+// caller buffer.
+namespace {
+
+// Size of the built-in scratch.  Every GPU that loads the library keeps this
+// much device memory until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uint8_t* rep,
+                                                        float global_scale, void* C, int64_t m,
+                                                        int64_t n, int64_t k,
+                                                        petit_stream_t stream) {
+  if (!(global_scale > 0.0f) || global_scale > 1.0e36f) return PETIT_ERR_INVALID_ARG;
+  if (!A || !rep || !C || m < 1) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(rep) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
+  int sms = 0;
+  if (petit_status_t st = current_device(&sms)) return st;
+  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, kNVFP4, sms);
+  if (plan.ws.total > kNoAllocScratchBytes) return PETIT_ERR_WORKSPACE;  // problem too large
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PETIT_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // first call on a device (with that device current): look up the
+    // array's device address -- in host code its name is only a host-side
+    // stand-in, never a device address
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return PETIT_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the status word and the arrival counters must start at zero; the array
+  // keeps whatever the previous call left in it
+  if (cudaMemsetAsync(scratch, 0, plan.ws.partials_off, s) != cudaSuccess) return PETIT_ERR_CUDA;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
+  petit::GemmArgs args{A, rep, C, m, n, k, global_scale * 256.0f, static_cast<uint8_t*>(scratch),
+                       kGemmTimeoutNs};
+  return from_cuda(petit::launch_gemm(plan, args, map, s));
+}

@@ -168,6 +168,32 @@ petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,
                                      void* workspace, size_t workspace_bytes,
                                      petit_stream_t stream);
 
+/* NVFP4 GEMM without a workspace argument.  The pages have no counterpart to
+ * this entry point; it is for callers that cannot allocate device memory at
+ * the time they call the GEMM: code running while a CUDA graph is being
+ * captured, plug-ins whose host framework owns all device memory, and
+ * latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  It computes what petit_gemm_bf16_nvfp4 computes, but its
+ * split-K scratch is an 8 MiB array built into the library's device image:
+ * every GPU that loads the library holds those 8 MiB until the process
+ * exits, and the call itself allocates and frees nothing.
+ *   - Problems whose scratch does not fit (on a 152-SM GB300: m > 32, for any
+ *     n, k) are rejected with PETIT_ERR_WORKSPACE; use the workspace entry
+ *     point for them.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Each call clears the scratch's status word and counters on `stream`
+ *     before its kernel.  All calls on a device share the one array, so calls
+ *     whose execution overlaps on the GPU (different streams, concurrent
+ *     graph branches) race and give wrong results: serialise them.
+ *   - Device-side wait time-outs of this variant are not reported (there is
+ *     no caller workspace to read them from).
+ * Arguments as for petit_gemm_bf16_nvfp4. */
+petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uint8_t* rep,
+                                             float global_scale, void* C,
+                                             int64_t m, int64_t n, int64_t k,
+                                             petit_stream_t stream);
+
 /* --------------------------------------------------------- error reporting */
 
 /* Waits for `stream`, reads the status word the kernels keep at the start of
