@@ -71,17 +71,18 @@ struct Cfg {
   static constexpr int kABytes = 2 * KU * kAHalfBytes;
   static constexpr int kWBytes = KU * T::kChunkBytes;          // codes + scales
   static constexpr int kStageBytes = kABytes + kWBytes;
-  static constexpr int kStages0 = (212 * 1024) / kStageBytes;
+  static constexpr int kStages0 = (220 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   static constexpr int kTx = kStageBytes;
-  static constexpr int kNumD = 2;                              // accumulator buffers (seg & 1)
+  // accumulator buffers: two (the epilogue of one tile overlaps the next), one at N = 256
+  static constexpr int kNumD = BN <= 128 ? 2 : 1;
   static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
   static constexpr int kNumA0 = (static_cast<int>(kTmemCols) - kNumD * BN) / kAColsPerUnit;
   static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
   static constexpr int kDColBase = kNumA * kAColsPerUnit;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kNumD * BN <= static_cast<int>(kTmemCols), "tensor memory");
   static_assert(kStages >= 2, "pipeline depth");
@@ -167,7 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
+      // weights are streamed once (evict first) unless several m-tiles
+      // revisit them, in which case the revisits should hit L2
+      const uint64_t policy = p.m_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
       // all per-unit indices advance incrementally: a runtime 64-bit division
       // costs hundreds of cycles in a single thread
       int64_t issued = 0;
@@ -215,8 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t u = u0; u < u1; ++u) {
         const bool first = (u == u0) || (ku == 0);
         const bool last = (u == u1 - 1) || (ku == KS - 1);
-        const int d = static_cast<int>(seg & 1);
-        if (first && !wait(&dempty[d], static_cast<uint32_t>(((seg >> 1) & 1) ^ 1))) break;
+        const int d = static_cast<int>(seg % C::kNumD);
+        if (first &&
+            !wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1)))
+          break;
         if (!wait(&full[st], ph)) break;
         if (!wait(&afull[b], pb)) break;
         tc_fence_after();
@@ -271,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t seg_end = (tile + 1) * KS < u1 ? (tile + 1) * KS : u1;
       const bool full_tile = (u == tile * KS) && (seg_end == (tile + 1) * KS);
       const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
-      const int d = static_cast<int>(seg & 1);
-      if (!wait(&dfull[d], static_cast<uint32_t>((seg >> 1) & 1))) break;
+      const int d = static_cast<int>(seg % C::kNumD);
+      if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
@@ -475,6 +480,7 @@ cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tma
     case 32: return launch_t<FMT, 32, 1>(prm, tmap, s);
     case 64: return launch_t<FMT, 64, 1>(prm, tmap, s);
     case 128: return launch_t<FMT, 128, 1>(prm, tmap, s);
+    case 256: return launch_t<FMT, 256, 1>(prm, tmap, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -486,7 +492,14 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
   GemmPlan pl{};
   pl.fmt = fmt;
-  pl.bn = m <= 16 ? 16 : (m <= 32 ? 32 : (m <= 64 ? 64 : 128));
+  pl.bn = m <= 16 ? 16 : (m <= 32 ? 32 : (m <= 64 ? 64 : (m <= 128 ? 128 : 256)));
+  if (pl.bn == 256 && m <= 256) {
+    // N = 256 dequantises each weight once for all rows, but halves the
+    // number of work units; small matrices keep two 128-row tiles so that
+    // every CTA still has a long pipeline to amortise its fixed costs over
+    const int64_t units256 = (n / kTileN) * (k / kStageK);
+    if (units256 < 48 * static_cast<int64_t>(num_sms)) pl.bn = 128;
+  }
   // two chunks per unit halves the copy requests when the A tile is small
   pl.ku = (pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
   pl.m_tiles = static_cast<int>((m + pl.bn - 1) / pl.bn);
