@@ -42,12 +42,13 @@
 namespace petit {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;
+constexpr int kMmaWarp = 1;     // tensor-memory owner and first MMA issuer
 constexpr int kEpiWarp0 = 2;    // warps 2..5
 constexpr int kDeqWarp0 = 6;    // warps 6..13
 constexpr int kNumDeqWarps = 8;
+constexpr int kMmaWarp2 = 14;   // second MMA issuer (another SM sub-partition)
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -74,17 +75,26 @@ struct Cfg {
   static constexpr int kStages0 = (220 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   static constexpr int kTx = kStageBytes;
-  // accumulator buffers: two (the epilogue of one tile overlaps the next), one at N = 256
-  static constexpr int kNumD = BN <= 128 ? 2 : 1;
+  // MMA-issuing threads.  One thread's issue + synchronisation loop cannot
+  // keep the tensor pipe busy with short (N <= 128) MMAs; two threads on
+  // different SM sub-partitions alternate units, each into its own
+  // accumulator, which the epilogue adds in a fixed order.
+  static constexpr int kMmaThreads = BN <= 128 ? 2 : 1;
   static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
-  static constexpr int kNumA0 = (static_cast<int>(kTmemCols) - kNumD * BN) / kAColsPerUnit;
+  // accumulator buffers per issuer: two when they fit beside three A-buffers
+  // (the epilogue of one tile then overlaps the next tile's MMAs)
+  static constexpr int kNumD =
+      kMmaThreads * 2 * BN + 3 * kAColsPerUnit <= static_cast<int>(kTmemCols) ? 2 : 1;
+  static constexpr int kNumA0 =
+      (static_cast<int>(kTmemCols) - kMmaThreads * kNumD * BN) / kAColsPerUnit;
   static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
-  static constexpr int kDColBase = kNumA * kAColsPerUnit;
+  static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kNumA >= 2, "tensor memory");
-  static_assert(kDColBase + kNumD * BN <= static_cast<int>(kTmemCols), "tensor memory");
+  static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
+                "tensor memory");
   static_assert(kStages >= 2, "pipeline depth");
 };
 
@@ -114,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* afull = mdone + C::kStages;
   uint64_t* dfull = afull + C::kNumA;
   uint64_t* dempty = dfull + C::kNumD;
-  uint64_t* fin = dempty + C::kNumD;
-  uint64_t* epi_bar = fin + 1;
+  uint64_t* fin = dempty + C::kNumD;   // one per MMA issuer
+  uint64_t* epi_bar = fin + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_flag = abort_flag + 1;
@@ -136,10 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
     for (int i = 0; i < C::kNumD; ++i) {
-      mbar_init(smem_u32(&dfull[i]), 1);
+      mbar_init(smem_u32(&dfull[i]), C::kMmaThreads);
       mbar_init(smem_u32(&dempty[i]), 4);
     }
-    mbar_init(smem_u32(fin), 1);
+    mbar_init(smem_u32(&fin[0]), 1);
+    mbar_init(smem_u32(&fin[1]), 1);
     mbar_init(smem_u32(epi_bar), 4);
     *abort_flag = 0;
     *epi_flag = 0;
@@ -154,6 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Programmatic dependent launch: the prologue above may overlap the tail of
+  // the previous kernel on the stream; nothing below touches global memory
+  // before that kernel has completed (its outputs may be A, or the weights).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   auto fail = [&]() {
     atomicOr(p.status, kStatusTimeout);
@@ -208,35 +224,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                             nullptr);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    const int t = warp == kMmaWarp ? 0 : 1;   // issuer index: units i with i % kMmaThreads == t
+    if (lane == 0 && t < C::kMmaThreads) {
       int64_t seg = 0;
       int st = 0, b = 0;
       uint32_t ph = 0, pb = 0;
       int64_t ku = u0 - (u0 / KS) * KS;
-      for (int64_t u = u0; u < u1; ++u) {
+      bool seg_started = false;   // this issuer has written its accumulator in this segment
+      int64_t i = 0;
+      for (int64_t u = u0; u < u1; ++u, ++i) {
         const bool first = (u == u0) || (ku == 0);
         const bool last = (u == u1 - 1) || (ku == KS - 1);
         const int d = static_cast<int>(seg % C::kNumD);
-        if (first &&
-            !wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1)))
-          break;
-        if (!wait(&full[st], ph)) break;
-        if (!wait(&afull[b], pb)) break;
-        tc_fence_after();
-        const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
-        const uint32_t d_tmem = tmem + C::kDColBase + d * BN;
-        const uint32_t a_tmem = tmem + b * C::kAColsPerUnit;
-#pragma unroll
-        for (int j = 0; j < KU * (kStageK / 16); ++j) {
-          // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
-          const uint64_t bdesc =
-              smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) + (((j & 3) * 32) >> 4);
-          mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc, (first && j == 0) ? 0u : 1u);
+        if (first) {
+          // Every issuer waits here, owning a unit of the segment or not: its
+          // dfull arrival for this segment then cannot overtake the other
+          // issuer's arrival for the segment that last used accumulator d.
+          seg_started = false;
+          if (!wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
         }
-        mma_commit(smem_u32(&mdone[st]));
+        if (i % C::kMmaThreads == t) {
+          if (!wait(&full[st], ph)) break;
+          if (!wait(&afull[b], pb)) break;
+          tc_fence_after();
+          const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
+          const uint32_t d_tmem = tmem + C::kDColBase + (t * C::kNumD + d) * BN;
+          const uint32_t a_tmem = tmem + b * C::kAColsPerUnit;
+#pragma unroll
+          for (int j = 0; j < KU * (kStageK / 16); ++j) {
+            // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
+            const uint64_t bdesc = smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) +
+                                   (((j & 3) * 32) >> 4);
+            mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
+                       (!seg_started && j == 0) ? 0u : 1u);
+          }
+          mma_commit(smem_u32(&mdone[st]));
+          seg_started = true;
+        }
         if (last) {
+          // every issuer arrives once per segment, when its MMAs are done
           mma_commit(smem_u32(&dfull[d]));
           ++seg;
         }
@@ -251,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ku == KS) ku = 0;
       }
       // all issued MMAs complete before tensor memory is released
-      mma_commit(smem_u32(fin));
-      mbar_wait_bounded(smem_u32(fin), 0, p.timeout_ns, nullptr);
+      mma_commit(smem_u32(&fin[t]));
+      mbar_wait_bounded(smem_u32(&fin[t]), 0, p.timeout_ns, nullptr);
     }
   } else if (warp < kDeqWarp0) {
     // ------------------------------------------------------------- epilogue
@@ -279,16 +307,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int d = static_cast<int>(seg % C::kNumD);
       if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
+      // issuer t wrote its accumulator iff the segment holds a unit with
+      // CTA-local index i % kMmaThreads == t
+      const int64_t seg_i0 = u - u0;
+      const bool has0 = C::kMmaThreads == 1 || (seg_end - u) >= 2 || (seg_i0 % 2) == 0;
+      const bool has1 = C::kMmaThreads == 2 && ((seg_end - u) >= 2 || (seg_i0 % 2) == 1);
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
+      const uint32_t tbase1 = tbase + C::kNumD * BN;   // issuer 1's accumulator
       const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
       const int64_t slot = 2 * cta + (tile == first_tile_of_cta ? 0 : 1);
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t v[16];
-        tmem_ld_x16(tbase + c0, v);
-        tmem_wait_ld();
+        if (has0) {
+          tmem_ld_x16(tbase + c0, v);
+          tmem_wait_ld();
+          if (has1) {
+            uint32_t w[16];
+            tmem_ld_x16(tbase1 + c0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[j]));
+          }
+        } else {
+          tmem_ld_x16(tbase1 + c0, v);
+          tmem_wait_ld();
+        }
         if (full_tile) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -462,6 +509,11 @@ cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t st
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN, KU>, prm, tmap);
 }
 

@@ -18,6 +18,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// -------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on (the previous kernel on the
+// stream) have completed and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next kernel on the stream to begin launching its blocks.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
