@@ -42,13 +42,13 @@
 namespace petit {
 namespace {
 
-constexpr int kThreads = 480;
 constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;     // tensor-memory owner and first MMA issuer
+constexpr int kMmaWarp = 1;     // tensor-memory owner and MMA issuer 0
 constexpr int kEpiWarp0 = 2;    // warps 2..5
 constexpr int kDeqWarp0 = 6;    // warps 6..13
 constexpr int kNumDeqWarps = 8;
-constexpr int kMmaWarp2 = 14;   // second MMA issuer (another SM sub-partition)
+constexpr int kMmaWarpX = 13;   // MMA issuer t >= 1 is warp 13 + t (warps 14, 15)
+constexpr int kMaxMmaThreads = 3;
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -74,12 +74,14 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kWBytes;
   static constexpr int kStages0 = (220 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
-  static constexpr int kTx = kStageBytes;
-  // MMA-issuing threads.  One thread's issue + synchronisation loop cannot
-  // keep the tensor pipe busy with short (N <= 128) MMAs; two threads on
-  // different SM sub-partitions alternate units, each into its own
-  // accumulator, which the epilogue adds in a fixed order.
-  static constexpr int kMmaThreads = BN <= 128 ? 2 : 1;
+  // MMA-issuing threads.  A thread issues one tcgen05.mma per ~65 cycles
+  // whatever N is, so short (N <= 128) MMAs need several issuers on
+  // different SM sub-partitions.  They take the CTA's units round-robin,
+  // each into its own accumulator, which the epilogue adds in a fixed order.
+  // Three issuers (warps 1, 14, 15 on sub-partitions 1, 2, 3) keep the CTA
+  // at 16 warps, four per sub-partition, so each thread may use 128 registers.
+  static constexpr int kMmaThreads = BN <= 32 ? 3 : BN <= 128 ? 2 : 1;
+  static constexpr int kThreads = 32 * (14 + kMmaThreads - 1);
   static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
   // accumulator buffers per issuer: two when they fit beside three A-buffers
   // (the epilogue of one tile then overlaps the next tile's MMAs)
@@ -89,12 +91,13 @@ struct Cfg {
       (static_cast<int>(kTmemCols) - kMmaThreads * kNumD * BN) / kAColsPerUnit;
   static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
                 "tensor memory");
+  static_assert(kMmaThreads <= kMaxMmaThreads, "issuers");
   static_assert(kStages >= 2, "pipeline depth");
 };
 
@@ -105,7 +108,7 @@ __device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t P) 
 }
 
 template <int FMT, int BN, int KU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_a) {
   using C = Cfg<FMT, BN, KU>;
   using T = FmtTraits<FMT>;
@@ -115,17 +118,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][BN][128 B]
   uint8_t* sm_w = sm_a + C::kStages * C::kABytes;          // [stage][KU chunks]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kStages * C::kWBytes);
-  // full[s]: the stage's copies landed.  mdone[s]: the MMAs of the unit in
-  // stage s completed -- which also means the dequantisers are done reading
-  // it (the MMAs only start after their tensor-memory stores), so one commit
-  // per unit frees both the stage and the unit's tensor-memory A-buffer.
-  uint64_t* full = bars;
-  uint64_t* mdone = full + C::kStages;
+  // Weights and activations of a unit share a stage index but have their
+  // own barriers, so each part is released as soon as its reader is done:
+  //   wfull[s] / wfree[s]: weight chunk landed / decoded by all dequantisers;
+  //   xfull[s] / mdone[s]: activation tile landed / the unit's MMAs completed
+  //   (mdone also frees the unit's tensor-memory A-buffer).
+  // The weights, the long HBM stream, so turn over a stage per unit without
+  // waiting for the tensor core.
+  uint64_t* wfull = bars;
+  uint64_t* wfree = wfull + C::kStages;
+  uint64_t* xfull = wfree + C::kStages;
+  uint64_t* mdone = xfull + C::kStages;
   uint64_t* afull = mdone + C::kStages;
   uint64_t* dfull = afull + C::kNumA;
   uint64_t* dempty = dfull + C::kNumD;
   uint64_t* fin = dempty + C::kNumD;   // one per MMA issuer
-  uint64_t* epi_bar = fin + 2;
+  uint64_t* epi_bar = fin + kMaxMmaThreads;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_flag = abort_flag + 1;
@@ -141,7 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&wfull[i]), 1);
+      mbar_init(smem_u32(&wfree[i]), kNumDeqWarps);
+      mbar_init(smem_u32(&xfull[i]), 1);
       mbar_init(smem_u32(&mdone[i]), 1);
     }
     for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
@@ -149,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&dfull[i]), C::kMmaThreads);
       mbar_init(smem_u32(&dempty[i]), 4);
     }
-    mbar_init(smem_u32(&fin[0]), 1);
-    mbar_init(smem_u32(&fin[1]), 1);
+    for (int i = 0; i < kMaxMmaThreads; ++i) mbar_init(smem_u32(&fin[i]), 1);
     mbar_init(smem_u32(epi_bar), 4);
     *abort_flag = 0;
     *epi_flag = 0;
@@ -187,54 +196,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weights are streamed once (evict first) unless several m-tiles
       // revisit them, in which case the revisits should hit L2
       const uint64_t policy = p.m_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
-      // all per-unit indices advance incrementally: a runtime 64-bit division
-      // costs hundreds of cycles in a single thread
-      int64_t issued = 0;
-      int st = 0;
-      uint32_t ph = 0;
+      // Two streams over the same units: weight chunks (stage freed by the
+      // dequantisers) and activation tiles (freed by the MMAs).  Whichever
+      // has a free stage is issued next, weights first.  All per-unit
+      // indices advance incrementally: a runtime 64-bit division costs
+      // hundreds of cycles in a single thread.
+      const int64_t nu = u1 - u0;
       const int64_t tile0 = u0 / KS;
-      int64_t ku = u0 - tile0 * KS;
-      int64_t nt = tile0 / p.m_tiles;
-      int64_t mt = tile0 - nt * p.m_tiles;
-      for (int64_t u = u0; u < u1; ++u, ++issued) {
-        if (!wait(&mdone[st], ph ^ 1u)) break;
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(fb, C::kTx);
-        bulk_g2s(smem_u32(sm_w + st * C::kWBytes),
-                 p.rep + chunk_offset<FMT>(nt, ku * KU, KS * KU), C::kWBytes, fb, policy);
-        tma_load_3d(smem_u32(sm_a + st * C::kABytes), &tmap_a, 0, static_cast<int32_t>(mt * BN),
-                    static_cast<int32_t>(ku * 2 * KU), fb);
-        if (++st == C::kStages) {
-          st = 0;
-          ph ^= 1u;
+      const int64_t ku0 = u0 - tile0 * KS;
+      int64_t wi = 0, xi = 0;           // next unit (CTA-local) of each stream
+      int ws = 0, xs = 0;               // their stages and phases
+      uint32_t wph = 0, xph = 0;
+      int64_t w_ku = ku0, w_nt = tile0 / p.m_tiles, w_mt = tile0 - w_nt * p.m_tiles;
+      int64_t x_ku = ku0, x_mt = w_mt;
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t spin = 0; wi < nu || xi < nu;) {
+        bool progress = false;
+        if (wi < nu && mbar_test_wait(smem_u32(&wfree[ws]), wph ^ 1u)) {
+          const uint32_t fb = smem_u32(&wfull[ws]);
+          mbar_arrive_expect_tx(fb, C::kWBytes);
+          bulk_g2s(smem_u32(sm_w + ws * C::kWBytes),
+                   p.rep + chunk_offset<FMT>(w_nt, w_ku * KU, KS * KU), C::kWBytes, fb, policy);
+          ++wi;
+          if (++ws == C::kStages) {
+            ws = 0;
+            wph ^= 1u;
+          }
+          if (++w_ku == KS) {
+            w_ku = 0;
+            if (++w_mt == p.m_tiles) {
+              w_mt = 0;
+              ++w_nt;
+            }
+          }
+          progress = true;
         }
-        if (++ku == KS) {
-          ku = 0;
-          if (++mt == p.m_tiles) {
-            mt = 0;
-            ++nt;
+        if (xi < nu && mbar_test_wait(smem_u32(&mdone[xs]), xph ^ 1u)) {
+          const uint32_t fb = smem_u32(&xfull[xs]);
+          mbar_arrive_expect_tx(fb, C::kABytes);
+          tma_load_3d(smem_u32(sm_a + xs * C::kABytes), &tmap_a, 0, static_cast<int32_t>(x_mt * BN),
+                      static_cast<int32_t>(x_ku * 2 * KU), fb);
+          ++xi;
+          if (++xs == C::kStages) {
+            xs = 0;
+            xph ^= 1u;
+          }
+          if (++x_ku == KS) {
+            x_ku = 0;
+            if (++x_mt == p.m_tiles) x_mt = 0;
+          }
+          progress = true;
+        }
+        if (!progress && (++spin & 63u) == 0) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > p.timeout_ns) {
+            fail();
+            break;
           }
         }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
-        const int64_t first = issued > C::kStages ? issued - C::kStages : 0;
-        for (int64_t j = first; j < issued; ++j)
-          mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, p.timeout_ns,
-                            nullptr);
+        const int64_t wfirst = wi > C::kStages ? wi - C::kStages : 0;
+        for (int64_t j = wfirst; j < wi; ++j)
+          mbar_wait_bounded(smem_u32(&wfull[j % C::kStages]), (j / C::kStages) & 1,
+                            p.timeout_ns, nullptr);
+        const int64_t xfirst = xi > C::kStages ? xi - C::kStages : 0;
+        for (int64_t j = xfirst; j < xi; ++j)
+          mbar_wait_bounded(smem_u32(&xfull[j % C::kStages]), (j / C::kStages) & 1,
+                            p.timeout_ns, nullptr);
       }
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+  } else if (warp == kMmaWarp || warp > kMmaWarpX) {
     // ------------------------------------------------------------ MMA issue
-    const int t = warp == kMmaWarp ? 0 : 1;   // issuer index: units i with i % kMmaThreads == t
-    if (lane == 0 && t < C::kMmaThreads) {
+    const int t = warp == kMmaWarp ? 0 : warp - kMmaWarpX;   // issues units i % kMmaThreads == t
+    if (lane == 0) {
       int64_t seg = 0;
       int st = 0, b = 0;
       uint32_t ph = 0, pb = 0;
       int64_t ku = u0 - (u0 / KS) * KS;
       bool seg_started = false;   // this issuer has written its accumulator in this segment
-      int64_t i = 0;
-      for (int64_t u = u0; u < u1; ++u, ++i) {
+      int owner = 0;   // CTA-local unit index modulo kMmaThreads
+      for (int64_t u = u0; u < u1; ++u) {
         const bool first = (u == u0) || (ku == 0);
         const bool last = (u == u1 - 1) || (ku == KS - 1);
         const int d = static_cast<int>(seg % C::kNumD);
@@ -245,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           seg_started = false;
           if (!wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
         }
-        if (i % C::kMmaThreads == t) {
-          if (!wait(&full[st], ph)) break;
+        if (owner == t) {
+          if (!wait(&xfull[st], ph)) break;
           if (!wait(&afull[b], pb)) break;
           tc_fence_after();
           const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
@@ -277,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb ^= 1u;
         }
         if (++ku == KS) ku = 0;
+        if (++owner == C::kMmaThreads) owner = 0;
       }
       // all issued MMAs complete before tensor memory is released
       mma_commit(smem_u32(&fin[t]));
@@ -309,32 +353,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // issuer t wrote its accumulator iff the segment holds a unit with
       // CTA-local index i % kMmaThreads == t
-      const int64_t seg_i0 = u - u0;
-      const bool has0 = C::kMmaThreads == 1 || (seg_end - u) >= 2 || (seg_i0 % 2) == 0;
-      const bool has1 = C::kMmaThreads == 2 && ((seg_end - u) >= 2 || (seg_i0 % 2) == 1);
+      const int seg_len = static_cast<int>(seg_end - u);
+      const int seg_r0 = static_cast<int>((u - u0) % C::kMmaThreads);
+      uint32_t has = 0;   // bit t: issuer t contributed
+#pragma unroll
+      for (int t = 0; t < C::kMmaThreads; ++t)
+        if ((t - seg_r0 + C::kMmaThreads) % C::kMmaThreads < seg_len) has |= 1u << t;
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
-      const uint32_t tbase1 = tbase + C::kNumD * BN;   // issuer 1's accumulator
       const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
       const int64_t slot = 2 * cta + (tile == first_tile_of_cta ? 0 : 1);
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
+        // the contributing accumulators, added in issuer order
         uint32_t v[16];
-        if (has0) {
-          tmem_ld_x16(tbase + c0, v);
-          tmem_wait_ld();
-          if (has1) {
+        bool have = false;
+#pragma unroll
+        for (int t = 0; t < C::kMmaThreads; ++t) {
+          if (has & (1u << t)) {
             uint32_t w[16];
-            tmem_ld_x16(tbase1 + c0, w);
+            tmem_ld_x16(tbase + (t * C::kNumD) * BN + c0, w);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[j]));
+              v[j] = have ? __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[j])) : w[j];
+            have = true;
           }
-        } else {
-          tmem_ld_x16(tbase1 + c0, v);
-          tmem_wait_ld();
         }
         if (full_tile) {
 #pragma unroll
@@ -417,23 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;         // tensor-memory lane quarter
     const int r = 32 * q + lane;    // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    // Two-deep software pipeline: the tensor-memory stores of unit i-1 are
-    // drained (wait::st) only after unit i has been loaded and decoded, so
-    // their latency overlaps useful work.
-    int prev_b = -1;
     int64_t i = 0;
     int st = 0, b = 0, st2 = 0;   // st2: stage of unit i - kNumA
     uint32_t ph = 0, ph2 = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
-      if (!wait(&full[st], ph)) break;
-      if (i >= C::kNumA) {
-        // A-buffer b was last used by unit i - kNumA: wait for its MMAs
-        if (!wait(&mdone[st2], ph2)) break;
-        if (++st2 == C::kStages) {
-          st2 = 0;
-          ph2 ^= 1u;
-        }
-      }
+      if (!wait(&wfull[st], ph)) break;
       uint4 g[KU][2];
       uint32_t sv[KU];
 #pragma unroll
@@ -457,11 +490,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode_group<FMT>(g[j][1], (sv[j] >> 8) & 0xFFu, o[j][1]);
         }
       }
-      if (prev_b >= 0) {
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[prev_b]));
+      // the decode consumed every byte this warp read: release the chunk
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
+      if (i >= C::kNumA) {
+        // A-buffer b was last used by unit i - kNumA: wait for its MMAs
+        if (!wait(&mdone[st2], ph2)) break;
+        if (++st2 == C::kStages) {
+          st2 = 0;
+          ph2 ^= 1u;
+        }
       }
 #pragma unroll
       for (int j = 0; j < KU; ++j) {
@@ -470,18 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x16(acol, o[j][0]);
         tmem_st_x16(acol + 16, o[j][1]);
       }
-      prev_b = b;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       if (++st == C::kStages) {
         st = 0;
         ph ^= 1u;
       }
       if (++b == C::kNumA) b = 0;
-    }
-    if (prev_b >= 0) {
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !*abort_flag) mbar_arrive(smem_u32(&afull[prev_b]));
     }
   }
 
@@ -506,7 +541,7 @@ cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t st
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_ctas));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
