@@ -47,6 +47,7 @@ constexpr int kMmaWarp = 1;     // tensor-memory owner and MMA issuer 0
 constexpr int kEpiWarp0 = 2;    // warps 2..5
 constexpr int kDeqWarp0 = 6;    // warps 6..13
 constexpr int kNumDeqWarps = 8;
+constexpr int kDeqGroupWarps = 4;   // one dequantiser group: a warp per lane quarter
 constexpr int kMmaWarpX = 13;   // MMA issuer t >= 1 is warp 13 + t (warps 14, 15)
 constexpr int kMaxMmaThreads = 3;
 constexpr uint32_t kTmemCols = 512;
@@ -89,7 +90,12 @@ struct Cfg {
       kMmaThreads * 2 * BN + 3 * kAColsPerUnit <= static_cast<int>(kTmemCols) ? 2 : 1;
   static constexpr int kNumA0 =
       (static_cast<int>(kTmemCols) - kMmaThreads * kNumD * BN) / kAColsPerUnit;
-  static constexpr int kNumA = kNumA0 > 4 ? 4 : kNumA0;        // dequantised-weight buffers
+  // Dequantised-weight buffers.  At most kStages: the dequantiser waits for
+  // mdone of unit i - kNumA on the barrier of that unit's stage, and no later
+  // unit i - kNumA + j*kStages < i may complete a phase there first (parity
+  // waits cannot tell two completed phases apart).
+  static constexpr int kNumA1 = kNumA0 > 4 ? 4 : kNumA0;
+  static constexpr int kNumA = kNumA1 > kStages ? kStages : kNumA1;
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
@@ -150,11 +156,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(&wfull[i]), 1);
-      mbar_init(smem_u32(&wfree[i]), kNumDeqWarps);
+      mbar_init(smem_u32(&wfree[i]), kDeqGroupWarps);
       mbar_init(smem_u32(&xfull[i]), 1);
       mbar_init(smem_u32(&mdone[i]), 1);
     }
-    for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kNumDeqWarps);
+    for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kDeqGroupWarps);
     for (int i = 0; i < C::kNumD; ++i) {
       mbar_init(smem_u32(&dfull[i]), C::kMmaThreads);
       mbar_init(smem_u32(&dempty[i]), 4);
@@ -457,8 +463,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     }
   } else {
     // ---------------------------------------------------------- dequantise
-    const int dw = warp - kDeqWarp0;
-    const int h = dw >> 2;          // which 64-k half of each chunk
+    // Two groups of four warps take alternate units; a warp decodes both
+    // 64-k halves of its 32 rows.  The two dequantiser warps of an SM
+    // sub-partition then work on different units, so one's barrier waits
+    // and round trips overlap the other's decode arithmetic.
+    const int grp = (warp - kDeqWarp0) / kDeqGroupWarps;
     const int q = warp & 3;         // tensor-memory lane quarter
     const int r = 32 * q + lane;    // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -466,57 +475,68 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     int st = 0, b = 0, st2 = 0;   // st2: stage of unit i - kNumA
     uint32_t ph = 0, ph2 = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
-      if (!wait(&wfull[st], ph)) break;
-      uint4 g[KU][2];
-      uint32_t sv[KU];
+      if ((i & 1) == grp) {
+        if (!wait(&wfull[st], ph)) break;
+        bool ok = true;
 #pragma unroll
-      for (int j = 0; j < KU; ++j) {
-        const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
-        g[j][0] = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
-        g[j][1] = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
-        if constexpr (FMT == kNVFP4)
-          sv[j] = *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
-        else
-          sv[j] = *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
-      }
-      uint32_t o[KU][2][16];
+        for (int h = 0; h < 2; ++h) {
+          uint4 g[KU][2];
+          uint32_t sv[KU];
 #pragma unroll
-      for (int j = 0; j < KU; ++j) {
-        if constexpr (FMT == kNVFP4) {
-          decode_group<FMT>(g[j][0], sv[j] & 0xFFFFu, o[j][0]);
-          decode_group<FMT>(g[j][1], sv[j] >> 16, o[j][1]);
-        } else {
-          decode_group<FMT>(g[j][0], sv[j] & 0xFFu, o[j][0]);
-          decode_group<FMT>(g[j][1], (sv[j] >> 8) & 0xFFu, o[j][1]);
+          for (int j = 0; j < KU; ++j) {
+            const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+            g[j][0] = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+            g[j][1] = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+            if constexpr (FMT == kNVFP4)
+              sv[j] = *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
+            else
+              sv[j] = *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
+          }
+          uint32_t o[KU][2][16];
+#pragma unroll
+          for (int j = 0; j < KU; ++j) {
+            if constexpr (FMT == kNVFP4) {
+              decode_group<FMT>(g[j][0], sv[j] & 0xFFFFu, o[j][0]);
+              decode_group<FMT>(g[j][1], sv[j] >> 16, o[j][1]);
+            } else {
+              decode_group<FMT>(g[j][0], sv[j] & 0xFFu, o[j][0]);
+              decode_group<FMT>(g[j][1], (sv[j] >> 8) & 0xFFu, o[j][1]);
+            }
+          }
+          if (h == 1) {
+            // the decode consumed every byte this warp read: release the chunk
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
+          } else if (i >= C::kNumA) {
+            // A-buffer b was last used by unit i - kNumA: wait for its MMAs
+            if (!wait(&mdone[st2], ph2)) {
+              ok = false;
+              break;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < KU; ++j) {
+            const uint32_t acol =
+                tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+            tmem_st_x16(acol, o[j][0]);
+            tmem_st_x16(acol + 16, o[j][1]);
+          }
         }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       }
-      // the decode consumed every byte this warp read: release the chunk
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
-      if (i >= C::kNumA) {
-        // A-buffer b was last used by unit i - kNumA: wait for its MMAs
-        if (!wait(&mdone[st2], ph2)) break;
-        if (++st2 == C::kStages) {
-          st2 = 0;
-          ph2 ^= 1u;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < KU; ++j) {
-        const uint32_t acol =
-            tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
-        tmem_st_x16(acol, o[j][0]);
-        tmem_st_x16(acol + 16, o[j][1]);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       if (++st == C::kStages) {
         st = 0;
         ph ^= 1u;
       }
       if (++b == C::kNumA) b = 0;
+      if (i >= C::kNumA && ++st2 == C::kStages) {
+        st2 = 0;
+        ph2 ^= 1u;
+      }
     }
   }
 

@@ -28,6 +28,14 @@ def _prep(cuda_lib, w, fmt, g=1.0):
     return codes, scales, cuda_lib.repack(wp, sp, fmt)
 
 
+def _gemm(cuda_lib, a, rep, n, fmt, g=1.0):
+    """One GEMM with its own workspace; no bounded wait may have run out."""
+    ws = cuda_lib.Workspace()
+    c = cuda_lib.gemm(a, rep, n, fmt, g, workspace=ws)
+    assert ws.status() == 0, "device status: a pipeline wait timed out"
+    return c
+
+
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
 @pytest.mark.parametrize("m,n,k", [(1024, 1024, 1024), (16, 256, 2048), (200, 384, 640)])
 def test_one_hot_is_bit_exact(cuda_lib, fmt, m, n, k):
@@ -36,7 +44,7 @@ def test_one_hot_is_bit_exact(cuda_lib, fmt, m, n, k):
     rng = np.random.default_rng(m + n + k)
     cols = rng.permutation(k)[:m] if m <= k else rng.integers(0, k, m)
     a = synth.one_hot_activations(m, k, cols).cuda()
-    c = cuda_lib.gemm(a, rep, n, fmt, 1.0)
+    c = _gemm(cuda_lib, a, rep, n, fmt, 1.0)
     torch.cuda.synchronize()
     wq_bits = ogemm.dequantize_bf16_bits(codes, scales, fmt)      # [n, k]
     expect = wq_bits[:, cols].T                                   # C[i, :] = Wq[:, cols[i]]
@@ -52,7 +60,7 @@ def test_nvfp4_parity_ragged_m(cuda_lib, m):
     w = synth.weights(n, k, seed=1)
     codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     a = synth.activations(m, k, seed=m)
-    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", 1.0)
+    c = _gemm(cuda_lib, a.cuda(), rep, n, "nvfp4", 1.0)
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), f"m={m}")
 
 
@@ -64,7 +72,7 @@ def test_odd_chunk_count(cuda_lib, fmt, m):
     w = synth.weights(n, k, seed=12)
     codes, scales, rep = _prep(cuda_lib, w, fmt)
     a = synth.activations(m, k, seed=13)
-    c = cuda_lib.gemm(a.cuda(), rep, n, fmt, 1.0)
+    c = _gemm(cuda_lib, a.cuda(), rep, n, fmt, 1.0)
     assert_parity(c, oracle_reference(a, codes, scales, fmt), f"m={m}")
 
 
@@ -74,7 +82,7 @@ def test_mxfp4_parity(cuda_lib, m):
     w = synth.weights(n, k, seed=2)
     codes, scales, rep = _prep(cuda_lib, w, "mxfp4")
     a = synth.activations(m, k, seed=10 + m)
-    c = cuda_lib.gemm(a.cuda(), rep, n, "mxfp4")
+    c = _gemm(cuda_lib, a.cuda(), rep, n, "mxfp4")
     assert_parity(c, oracle_reference(a, codes, scales, "mxfp4"), f"m={m}")
 
 
@@ -86,7 +94,7 @@ def test_nvfp4_global_scale_and_outliers(cuda_lib, m):
     g = float(quantize.nvfp4_global_scale(w.float().numpy()))
     codes, scales, rep = _prep(cuda_lib, w, "nvfp4", g)
     a = synth.activations(m, k, seed=4, outlier_frac=0.001, outlier_std=20.0)
-    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", g)
+    c = _gemm(cuda_lib, a.cuda(), rep, n, "nvfp4", g)
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4", g), f"m={m}")
 
 
@@ -95,17 +103,17 @@ def test_special_cases(cuda_lib):
     w = synth.weights(n, k, seed=6)
     codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
     z = torch.zeros((7, k), dtype=torch.bfloat16, device="cuda")
-    c = cuda_lib.gemm(z, rep, n, "nvfp4")
+    c = _gemm(cuda_lib, z, rep, n, "nvfp4")
     assert torch.all(c == 0)
     # all-zero weights (zero codes, smallest positive scale)
     zw = torch.zeros((n, k), dtype=torch.bfloat16)
     codes0, scales0, rep0 = _prep(cuda_lib, zw, "nvfp4")
     assert np.all(codes0 == 0)
     a = synth.activations(9, k, seed=7).cuda()
-    assert torch.all(cuda_lib.gemm(a, rep0, n, "nvfp4") == 0)
+    assert torch.all(_gemm(cuda_lib, a, rep0, n, "nvfp4") == 0)
     # all-ones activations give (BF16-rounded) row sums
     ones = torch.ones((1, k), dtype=torch.bfloat16, device="cuda")
-    assert_parity(cuda_lib.gemm(ones, rep, n, "nvfp4"),
+    assert_parity(_gemm(cuda_lib, ones, rep, n, "nvfp4"),
                   oracle_reference(ones.cpu(), codes, scales, "nvfp4"), "ones")
 
 
@@ -143,3 +151,40 @@ def test_bounded_wait_reports_timeout(cuda_lib):
     c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", workspace=ws)
     assert ws.status() == 0
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), "after timeout")
+
+
+# m -> the kernel's activation tile N (16/32/64/128/256) and chunks per unit;
+# k/128 odd forces one chunk per unit.  Repeated launches catch pipeline
+# races (a lost or aliased barrier phase shows up as a timeout status or a
+# changed result).
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("m,k", [(8, 4096), (24, 4096), (48, 4096), (48, 3968), (100, 4096),
+                                 (200, 4096), (300, 2048), (16, 3968)])
+def test_every_tile_config_repeated(cuda_lib, fmt, m, k):
+    n = 2048
+    w = synth.weights(n, k, seed=m + k)
+    codes, scales, rep = _prep(cuda_lib, w, fmt)
+    a = synth.activations(m, k, seed=m).cuda()
+    ws = cuda_lib.Workspace()
+    first = cuda_lib.gemm(a, rep, n, fmt, 1.0, workspace=ws).clone()
+    for _ in range(12):
+        again = cuda_lib.gemm(a, rep, n, fmt, 1.0, workspace=ws)
+        assert torch.equal(again, first)
+    assert ws.status() == 0
+    rows = np.arange(0, n, 37)
+    assert_parity(first[:, rows], oracle_reference(a.cpu(), codes[rows], scales[rows], fmt), f"m={m}")
+
+
+def test_large_prefill_tile(cuda_lib):
+    """m = 256 on a matrix large enough for 256-row activation tiles (one
+    dequantisation per weight for all rows); oracle on sampled columns."""
+    m, n, k = 256, 8192, 16384
+    w = synth.weights(n, k, seed=31, device="cuda")
+    wp, sp = cuda_lib.quantize(w, "nvfp4", 1.0)
+    rep = cuda_lib.repack(wp, sp, "nvfp4")
+    a = synth.activations(m, k, seed=32, outlier_frac=0.001, outlier_std=20.0).cuda()
+    c = _gemm(cuda_lib, a, rep, n, "nvfp4", 1.0)
+    rows = np.concatenate([np.arange(0, 256, 5), np.arange(n - 300, n, 7)])
+    # quantisation is row-local: the oracle quantises just the sampled rows
+    codes, scales = oracle_quantize(w[rows].cpu(), "nvfp4", 1.0)
+    assert_parity(c[:, rows], oracle_reference(a.cpu(), codes, scales, "nvfp4"), "m=256 large")
