@@ -72,9 +72,6 @@ struct Cfg {
   static constexpr int kAHalfBytes = BN * 128;                 // one 64-k slab, BN rows
   static constexpr int kABytes = 2 * KU * kAHalfBytes;
   static constexpr int kWBytes = KU * T::kChunkBytes;          // codes + scales
-  static constexpr int kStageBytes = kABytes + kWBytes;
-  static constexpr int kStages0 = (220 * 1024) / kStageBytes;
-  static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   // MMA-issuing threads.  A thread issues one tcgen05.mma per ~65 cycles
   // whatever N is, so short (N <= 128) MMAs need several issuers on
   // different SM sub-partitions.  They take the CTA's units round-robin,
@@ -90,21 +87,42 @@ struct Cfg {
       kMmaThreads * 2 * BN + 3 * kAColsPerUnit <= static_cast<int>(kTmemCols) ? 2 : 1;
   static constexpr int kNumA0 =
       (static_cast<int>(kTmemCols) - kMmaThreads * kNumD * BN) / kAColsPerUnit;
-  // Dequantised-weight buffers.  At most kStages: the dequantiser waits for
-  // mdone of unit i - kNumA on the barrier of that unit's stage, and no later
-  // unit i - kNumA + j*kStages < i may complete a phase there first (parity
-  // waits cannot tell two completed phases apart).
-  static constexpr int kNumA1 = kNumA0 > 4 ? 4 : kNumA0;
-  static constexpr int kNumA = kNumA1 > kStages ? kStages : kNumA1;
+  // Every mbarrier is waited on by one fixed consumer that waits for each of
+  // its phases in turn: a parity wait cannot tell phase j from phase j + 2,
+  // so a consumer that skipped a phase could pass a wait on a phase that has
+  // not completed.  The two dequantiser groups take units by parity, the
+  // MMA issuers by unit index modulo kMmaThreads; hence
+  //   * kWStages is even (a weight stage always holds units of one parity);
+  //   * kXStages is a multiple of kMmaThreads (an activation stage always
+  //     feeds the same issuer) and, with several issuers, even: the
+  //     dequantisers also wait on the activation stage's mdone barrier to
+  //     reuse an A-buffer, so its units must belong to one group;
+  //   * kNumA is a multiple of kMmaThreads (an A-buffer always feeds the
+  //     same issuer) and at most kXStages: the dequantiser waits for mdone of
+  //     unit i - kNumA, and no later unit sharing that barrier may complete
+  //     first.
+  static constexpr int kXMult = kMmaThreads == 3 ? 6 : kMmaThreads;
+  static constexpr int kXBudget = BN >= 256 ? 192 * 1024 : (BN <= 32 ? 96 * 1024 : 128 * 1024);
+  static constexpr int kXStages0 = (kXBudget / kABytes) / kXMult * kXMult;
+  static constexpr int kXStages = kXStages0 > 16 ? 16 / kXMult * kXMult : kXStages0;
+  static constexpr int kRingBytes = 220 * 1024;
+  static constexpr int kWStages0 = (kRingBytes - kXStages * kABytes) / kWBytes / 2 * 2;
+  static constexpr int kWStages = kWStages0 > 12 ? 12 : kWStages0;
+  static constexpr int kNumA1 = (kNumA0 > 4 ? 4 : kNumA0) / kMmaThreads * kMmaThreads;
+  static constexpr int kNumA = kNumA1 > kXStages ? kXStages / kMmaThreads * kMmaThreads : kNumA1;
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
+  static constexpr int kSmemBytes = 1024 + kXStages * kABytes + kWStages * kWBytes + 1024;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
                 "tensor memory");
   static_assert(kMmaThreads <= kMaxMmaThreads, "issuers");
-  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kWStages >= 2 && kXStages >= 2 && kWStages % 2 == 0, "pipeline depth");
+  static_assert(kXStages % kMmaThreads == 0 && (kMmaThreads == 1 || kXStages % 2 == 0) &&
+                    kNumA % kMmaThreads == 0 && kNumA <= kXStages,
+                "fixed consumer per barrier");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 // CTA that owns stream-K unit u when U units are split over P CTAs with
@@ -122,8 +140,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][BN][128 B]
-  uint8_t* sm_w = sm_a + C::kStages * C::kABytes;          // [stage][KU chunks]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kStages * C::kWBytes);
+  uint8_t* sm_w = sm_a + C::kXStages * C::kABytes;         // [stage][KU chunks]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kWStages * C::kWBytes);
   // Weights and activations of a unit share a stage index but have their
   // own barriers, so each part is released as soon as its reader is done:
   //   wfull[s] / wfree[s]: weight chunk landed / decoded by all dequantisers;
@@ -132,10 +150,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   // The weights, the long HBM stream, so turn over a stage per unit without
   // waiting for the tensor core.
   uint64_t* wfull = bars;
-  uint64_t* wfree = wfull + C::kStages;
-  uint64_t* xfull = wfree + C::kStages;
-  uint64_t* mdone = xfull + C::kStages;
-  uint64_t* afull = mdone + C::kStages;
+  uint64_t* wfree = wfull + C::kWStages;
+  uint64_t* xfull = wfree + C::kWStages;
+  uint64_t* mdone = xfull + C::kXStages;
+  uint64_t* afull = mdone + C::kXStages;
   uint64_t* dfull = afull + C::kNumA;
   uint64_t* dempty = dfull + C::kNumD;
   uint64_t* fin = dempty + C::kNumD;   // one per MMA issuer
@@ -154,9 +172,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   const int64_t KS = p.k_units;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < C::kWStages; ++i) {
       mbar_init(smem_u32(&wfull[i]), 1);
       mbar_init(smem_u32(&wfree[i]), kDeqGroupWarps);
+    }
+    for (int i = 0; i < C::kXStages; ++i) {
       mbar_init(smem_u32(&xfull[i]), 1);
       mbar_init(smem_u32(&mdone[i]), 1);
     }
@@ -224,7 +244,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           bulk_g2s(smem_u32(sm_w + ws * C::kWBytes),
                    p.rep + chunk_offset<FMT>(w_nt, w_ku * KU, KS * KU), C::kWBytes, fb, policy);
           ++wi;
-          if (++ws == C::kStages) {
+          if (++ws == C::kWStages) {
             ws = 0;
             wph ^= 1u;
           }
@@ -243,7 +263,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           tma_load_3d(smem_u32(sm_a + xs * C::kABytes), &tmap_a, 0, static_cast<int32_t>(x_mt * BN),
                       static_cast<int32_t>(x_ku * 2 * KU), fb);
           ++xi;
-          if (++xs == C::kStages) {
+          if (++xs == C::kXStages) {
             xs = 0;
             xph ^= 1u;
           }
@@ -263,13 +283,13 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
-        const int64_t wfirst = wi > C::kStages ? wi - C::kStages : 0;
+        const int64_t wfirst = wi > C::kWStages ? wi - C::kWStages : 0;
         for (int64_t j = wfirst; j < wi; ++j)
-          mbar_wait_bounded(smem_u32(&wfull[j % C::kStages]), (j / C::kStages) & 1,
+          mbar_wait_bounded(smem_u32(&wfull[j % C::kWStages]), (j / C::kWStages) & 1,
                             p.timeout_ns, nullptr);
-        const int64_t xfirst = xi > C::kStages ? xi - C::kStages : 0;
+        const int64_t xfirst = xi > C::kXStages ? xi - C::kXStages : 0;
         for (int64_t j = xfirst; j < xi; ++j)
-          mbar_wait_bounded(smem_u32(&xfull[j % C::kStages]), (j / C::kStages) & 1,
+          mbar_wait_bounded(smem_u32(&xfull[j % C::kXStages]), (j / C::kXStages) & 1,
                             p.timeout_ns, nullptr);
       }
     }
@@ -317,7 +337,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           mma_commit(smem_u32(&dfull[d]));
           ++seg;
         }
-        if (++st == C::kStages) {
+        if (++st == C::kXStages) {
           st = 0;
           ph ^= 1u;
         }
@@ -412,9 +432,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         __threadfence();
         if (!epi_sync()) break;
         if (epi_tid == 0) {
-          const uint32_t old = atomicAdd(&p.counters[tile], 1u);
+          // acq_rel at GPU scope: releases the partials this CTA's epilogue
+          // threads stored (ordered before this point by their fences and
+          // the group barrier) and acquires those of earlier arrivals
+          const uint32_t old = atomic_add_acq_rel_gpu(&p.counters[c_first], 1u);
           const int is_last = (static_cast<int64_t>(old) == c_last - c_first);
-          if (is_last) atomicExch(&p.counters[tile], 0u);  // ready for the next call
+          if (is_last) atomicExch(&p.counters[c_first], 0u);  // ready for the next call
           *epi_flag = is_last;
         }
         if (!epi_sync()) break;
@@ -508,11 +531,13 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
           } else if (i >= C::kNumA) {
-            // A-buffer b was last used by unit i - kNumA: wait for its MMAs
+            // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
+            // and order the stores below after their operand reads
             if (!wait(&mdone[st2], ph2)) {
               ok = false;
               break;
             }
+            tc_fence_after();
           }
 #pragma unroll
           for (int j = 0; j < KU; ++j) {
@@ -528,12 +553,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       }
-      if (++st == C::kStages) {
+      if (++st == C::kWStages) {
         st = 0;
         ph ^= 1u;
       }
       if (++b == C::kNumA) b = 0;
-      if (i >= C::kNumA && ++st2 == C::kStages) {
+      if (i >= C::kNumA && ++st2 == C::kXStages) {
         st2 = 0;
         ph2 ^= 1u;
       }
@@ -615,9 +640,9 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
   pl.units = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles * (pl.k_stages / pl.ku);
   pl.num_ctas = static_cast<int>(pl.units < num_sms ? pl.units : num_sms);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
+  if (pl.num_ctas > kMaxCtas) pl.num_ctas = kMaxCtas;
   pl.ws.counters_off = kWsHeaderBytes;
-  pl.ws.partials_off = align_up(
-      pl.ws.counters_off + sizeof(uint32_t) * static_cast<size_t>(pl.n_tiles) * pl.m_tiles, 256);
+  pl.ws.partials_off = align_up(kWsHeaderBytes + kWsCountersBytes, 256);
   pl.ws.total = pl.ws.partials_off +
                 sizeof(float) * 2ull * static_cast<size_t>(pl.num_ctas) * pl.bn * kTileN;
   return pl;

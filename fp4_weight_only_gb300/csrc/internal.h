@@ -10,9 +10,16 @@ namespace petit {
 
 constexpr uint32_t kStatusTimeout = 1u;  // bit in the workspace status word
 
-// Workspace: [0, 256) status word and reserved; then per-tile arrival
-// counters (u32); then FP32 split-K partial slots, two per CTA.
+// Workspace: [0, 256) status word and reserved; [256, 4352) split-tile
+// arrival counters (u32), one per CTA index -- a split tile counts on the
+// counter of its first contributing CTA, and a CTA is the first contributor
+// of at most one split tile (the last tile of its range); then FP32 split-K
+// partial slots, two per CTA.  The counter region has the same place and
+// size for every problem, so no call's partials ever land on another
+// call's counters and a workspace can be shared by problems of any shape.
 constexpr size_t kWsHeaderBytes = 256;
+constexpr int kMaxCtas = 1024;
+constexpr size_t kWsCountersBytes = sizeof(uint32_t) * kMaxCtas;
 
 struct WsLayout {
   size_t counters_off;

@@ -88,6 +88,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------- copies
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

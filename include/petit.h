@@ -78,12 +78,13 @@ const char* petit_status_string(petit_status_t status);
  * n*k/32 (MXFP4) scale bytes; 0 for an unknown format. */
 size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt);
 
-/* Bytes of GEMM workspace for this problem on the current device (holds a
- * device status word, per-tile arrival counters and FP32 split-K partials).
- * Returns 0 if the arguments are invalid or no device is usable.  A
- * workspace must be zero-filled once after allocation; every successful
- * GEMM leaves it in that state again, so it can be reused by later calls of
- * any size that fits. */
+/* Bytes of GEMM workspace for this problem on the current device: a device
+ * status word, split-tile arrival counters (a fixed 4096-byte region) and
+ * FP32 split-K partials.  Returns 0 if the arguments are invalid or no
+ * device is usable.  A workspace must be zero-filled once after allocation;
+ * every successful GEMM leaves the status word and the counters at zero
+ * again (the partials region holds scratch data), so it can be reused by
+ * later calls of any shape that fits. */
 size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt);
 
 /* ------------------------------------------------------ offline weight prep */
