@@ -369,24 +369,83 @@ def run_ours(args, rank, world, local):
            "path": "binding.gemm (ctypes -> C ABI) per layer, eager, pinned host buffers"}
 
     # prefill m = 256 (same kernels, tcgen05 N = 128 tiles), per-GEMM timing
-    prefill = None
-    if not args.no_prefill:
-        pa = [synth.activations(M_PREFILL, k, seed=300 + i, device=dev, outlier_frac=0.001)
-              for i, (_, n, k) in enumerate(SHAPES)]
-        pc = [torch.empty((M_PREFILL, n), dtype=torch.bfloat16, device=dev) for _, n, _ in SHAPES]
-        for i in range(len(SHAPES)):
-            for which in (0, 1):
-                launch(i, which, M_PREFILL, pa[i], pc[i])
-        torch.cuda.synchronize()
-        pre_ms = shape_durations(
-            [[(lambda i=i, w=w: launch(i, w, M_PREFILL, pa[i], pc[i])) for w in (0, 1)]
-             for i in range(len(SHAPES))], stream, 10)
-        prefill = {}
+    def prepared(fmt, seed0, gscale):
+        """Two copies of the four weights in `fmt` (g = amax/(6*448) per
+        matrix if gscale), with their global scales."""
+        reps, gs = [[], []], []
         for i, (name, n, k) in enumerate(SHAPES):
-            t = pre_ms[i] * 1e-3
-            tf = 2 * M_PREFILL * n * k / t / 1e12
-            prefill[name] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
-                             "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+            w = synth.weights(n, k, seed=seed0 + i, device=dev)
+            g = binding.nvfp4_global_scale(binding.absmax(w).item()) if gscale else 1.0
+            fw = binding.FP4Weight(w, fmt, g)
+            del w
+            reps[0].append(fw.rep)
+            reps[1].append(fw.rep.clone())
+            gs.append(g)
+        return reps, gs
+
+    def shape_table(fmt, reps, gs, m, seed0, outliers=0.0, burst_reps=10):
+        a = [synth.activations(m, k, seed=seed0 + i, device=dev, outlier_frac=outliers)
+             for i, (_, n, k) in enumerate(SHAPES)]
+        c = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for _, n, _ in SHAPES]
+
+        def fn(i, w):
+            binding.gemm(a[i], reps[w][i], SHAPES[i][1], fmt, gs[i], workspace=ws, out=c[i])
+        for i in range(len(SHAPES)):
+            ws.ensure(binding.workspace_bytes(m, SHAPES[i][1], SHAPES[i][2], fmt))
+            for w in (0, 1):
+                fn(i, w)
+        torch.cuda.synchronize()
+        ms = shape_durations([[(lambda i=i, w=w: fn(i, w)) for w in (0, 1)] for i in range(len(SHAPES))],
+                             stream, burst_reps)
+        out = {}
+        for i, (name, n, k) in enumerate(SHAPES):
+            t = ms[i] * 1e-3
+            b = algo_bytes(m, n, k, 16 if fmt == "nvfp4" else 32)
+            tf = 2 * m * n * k / t / 1e12
+            out[name] = {"us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 2),
+                         "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3),
+                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+        out["step_us"] = round(float(ms.sum()) * 1e3, 2)
+        return out
+
+    prefill = None
+    mxfp4 = None
+    m_sweep = None
+    if not args.no_prefill:
+        # NVFP4 prefill: m = 256, 0.1 % N(0,20) activation outliers, g = amax/(6*448)
+        reps_g, gs_g = prepared("nvfp4", 500, True)
+        prefill = shape_table("nvfp4", reps_g, gs_g, M_PREFILL, 300, outliers=0.001)
+        del reps_g
+        # MXFP4 decode variant at m in {1, 4, 8, 16}
+        reps_mx, gs_mx = prepared("mxfp4", 600, False)
+        mxfp4 = {f"m={m}": shape_table("mxfp4", reps_mx, gs_mx, m, 700 + m) for m in (1, 4, 8, 16)}
+        del reps_mx
+        # NVFP4 m sweep at n = k = 8192 (two weight copies), and m = n = k = 4096
+        m_sweep = {}
+        for (n, k, ms_list) in ((8192, 8192, (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)), (4096, 4096, (4096,))):
+            wsq = synth.weights(n, k, seed=800 + n, device=dev)
+            f0 = binding.FP4Weight(wsq, "nvfp4", 1.0)
+            del wsq
+            r2 = [f0.rep, f0.rep.clone()]
+            for m in ms_list:
+                a = synth.activations(m, k, seed=900 + m, device=dev)
+                c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                ws.ensure(binding.workspace_bytes(m, n, k))
+
+                def fn(w, a=a, c=c, n=n):
+                    binding.gemm(a, r2[w], n, "nvfp4", 1.0, workspace=ws, out=c)
+                fn(0); fn(1)
+                torch.cuda.synchronize()
+                t = float(shape_durations([[lambda: fn(0), lambda: fn(1)]], stream, 10)[0]) * 1e-3
+                b = algo_bytes(m, n, k)
+                tf = 2 * m * n * k / t / 1e12
+                roof_t = max(b / (peaks["hbm_gbs"] * 1e9), 2 * m * n * k / (peaks["bf16_tflops"] * 1e12))
+                m_sweep[f"m={m} n={n} k={k}"] = {
+                    "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 1),
+                    "bound": "hbm" if b / (peaks["hbm_gbs"] * 1e9) >= 2 * m * n * k / (peaks["bf16_tflops"] * 1e12)
+                    else "tensor",
+                    "frac_roofline": round(roof_t / t, 3)}
+            del f0, r2
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -412,7 +471,8 @@ def run_ours(args, rank, world, local):
                        "parallelism": f"replicas x{world}"},
             "tflops": round(world * step_flops * args.steps / (elapsed_max * 1e-3) / 1e12, 2),
             "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
-            "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks, "prefill_m256": prefill,
+            "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
+            "prefill_m256": prefill, "mxfp4_decode": mxfp4, "m_sweep": m_sweep,
         }
         print(json.dumps(out), flush=True)
 
