@@ -411,6 +411,7 @@ def run_ours(args, rank, world, local):
     prefill = None
     mxfp4 = None
     m_sweep = None
+    cublas = None
     if not args.no_prefill:
         # NVFP4 prefill: m = 256, 0.1 % N(0,20) activation outliers, g = amax/(6*448)
         reps_g, gs_g = prepared("nvfp4", 500, True)
@@ -446,6 +447,24 @@ def run_ours(args, rank, world, local):
                     else "tensor",
                     "frac_roofline": round(roof_t / t, 3)}
             del f0, r2
+        # context row: cuBLAS BF16 dense GEMM on the same shapes (BF16 weights are
+        # 3.6x the NVFP4 bytes; two copies alternate so they come from HBM too)
+        cublas = {}
+        for i, (name, n, k) in enumerate(SHAPES):
+            wb = [synth.weights(n, k, seed=950 + i + 10 * c, device=dev) for c in (0, 1)]
+            row = {}
+            for m in (M_DECODE, M_PREFILL):
+                a = synth.activations(m, k, seed=960 + m, device=dev)
+                fns = [lambda c=c, a=a: torch.matmul(a, wb[c].t()) for c in (0, 1)]
+                for f in fns:
+                    f()
+                torch.cuda.synchronize()
+                t = float(shape_durations([fns], stream, 10)[0]) * 1e-3
+                ours = (per_kernel_ms[i] * 1e-3) if m == M_DECODE else prefill[name]["us"] * 1e-6
+                row[f"m={m}"] = {"us": round(t * 1e6, 2), "tflops": round(2 * m * n * k / t / 1e12, 1),
+                                 "ours_speedup": round(t / ours, 2)}
+            cublas[name] = row
+            del wb
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -473,6 +492,7 @@ def run_ours(args, rank, world, local):
             "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
             "prefill_m256": prefill, "mxfp4_decode": mxfp4, "m_sweep": m_sweep,
+            "cublas_bf16_context": cublas,
         }
         print(json.dumps(out), flush=True)
 

@@ -53,6 +53,8 @@ SIGNATURES = {
                                              _c_p, _c_sz, _c_p]),
     "petit_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_sz,
                                              _c_p]),
+    "petit_gemm_bf16_nvfp4_dscale": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                                    _c_p, _c_sz, _c_p]),
     "petit_gemm_bf16_nvfp4_noalloc": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
                                                      _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
@@ -179,7 +181,9 @@ class Workspace:
 
 
 def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
-    """C[m, n] = g * A @ dequant(W)^T in BF16 (FP32 accumulation)."""
+    """C[m, n] = g * A @ dequant(W)^T in BF16 (FP32 accumulation).  For NVFP4,
+    `global_scale` is a float or a one-element FP32 CUDA tensor (read by the
+    kernel, so a CUDA graph picks up a changed value on replay)."""
     _need(A, torch.bfloat16, "A")
     m, k = A.shape
     ws = workspace or Workspace(A.device)
@@ -189,7 +193,11 @@ def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
     buf = ws.ensure(need)
     C = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=A.device)
     L = load()
-    if fmt == "nvfp4":
+    if fmt == "nvfp4" and isinstance(global_scale, torch.Tensor):
+        _need(global_scale, torch.float32, "global_scale")
+        st = L.petit_gemm_bf16_nvfp4_dscale(_ptr(A), _ptr(rep), _ptr(global_scale), _ptr(C),
+                                            m, n, k, _ptr(buf), buf.numel(), _stream())
+    elif fmt == "nvfp4":
         st = L.petit_gemm_bf16_nvfp4(_ptr(A), _ptr(rep), ctypes.c_float(global_scale), _ptr(C),
                                      m, n, k, _ptr(buf), buf.numel(), _stream())
     else:

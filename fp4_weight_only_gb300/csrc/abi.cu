@@ -101,7 +101,7 @@ petit_status_t check_tiled_shape(int64_t n, int64_t k) {
 
 petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alpha, void* C,
                            int64_t m, int64_t n, int64_t k, void* ws, size_t ws_bytes,
-                           petit_stream_t stream) {
+                           petit_stream_t stream, const float* alpha_dev = nullptr) {
   if (!A || !rep || !C || m < 1) return PETIT_ERR_INVALID_ARG;
   if (petit_status_t st = check_tiled_shape(n, k)) return st;
   if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
@@ -116,6 +116,10 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   std::memset(&map, 0, sizeof(map));
   if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
   petit::GemmArgs args{A, rep, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  if (alpha_dev) {
+    args.alpha_dev = alpha_dev;
+    args.alpha_scale = alpha;
+  }
   return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -227,6 +231,16 @@ petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* rep, float gl
   // the register decode yields Wq * 2^-8; the epilogue restores it with g
   return gemm_common(kNVFP4, A, rep, global_scale * 256.0f, C, m, n, k, workspace,
                      workspace_bytes, stream);
+}
+
+petit_status_t petit_gemm_bf16_nvfp4_dscale(const void* A, const uint8_t* rep,
+                                            const float* global_scale_dev, void* C, int64_t m,
+                                            int64_t n, int64_t k, void* workspace,
+                                            size_t workspace_bytes, petit_stream_t stream) {
+  if (!global_scale_dev || reinterpret_cast<uintptr_t>(global_scale_dev) % 4 != 0)
+    return PETIT_ERR_INVALID_ARG;
+  return gemm_common(kNVFP4, A, rep, 256.0f, C, m, n, k, workspace, workspace_bytes, stream,
+                     global_scale_dev);
 }
 
 petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C, int64_t m,

@@ -64,6 +64,8 @@ struct Params {
   int32_t num_ctas;
   float alpha;
   uint64_t timeout_ns;
+  const float* alpha_dev;   // nullable: device-resident factor, times alpha_scale
+  float alpha_scale;
 };
 
 template <int FMT, int BN, int KU>
@@ -359,6 +361,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
     int64_t seg = 0;
     const int64_t first_tile_of_cta = u0 / KS;
+    // epilogue factor: a device-resident global scale is read here, after the
+    // grid dependency wait, so a preceding kernel may have produced it
+    const float alpha = p.alpha_dev ? p.alpha_scale * *p.alpha_dev : p.alpha;
     uint32_t epi_phase = 0;
     // bounded barrier among the four epilogue warps (a hardware named
     // barrier has no time limit)
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           for (int j = 0; j < 16; ++j) {
             const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
             if (mrow < p.m)
-              p.c[mrow * p.n + ncol] = __float2bfloat16_rn(p.alpha * __uint_as_float(v[j]));
+              p.c[mrow * p.n + ncol] = __float2bfloat16_rn(alpha * __uint_as_float(v[j]));
           }
         } else {
 #pragma unroll
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-              if (mrow < p.m) p.c[mrow * p.n + ncol] = __float2bfloat16_rn(p.alpha * acc[j]);
+              if (mrow < p.m) p.c[mrow * p.n + ncol] = __float2bfloat16_rn(alpha * acc[j]);
             }
           }
         }
@@ -663,6 +668,8 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   prm.units = pl.units;
   prm.num_ctas = pl.num_ctas;
   prm.alpha = a.alpha;
+  prm.alpha_dev = a.alpha_dev;
+  prm.alpha_scale = a.alpha_scale;
   prm.timeout_ns = a.timeout_ns;
   if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream);
   return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream);

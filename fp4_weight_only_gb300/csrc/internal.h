@@ -49,6 +49,10 @@ struct GemmArgs {
   float alpha;
   uint8_t* workspace;
   uint64_t timeout_ns;
+  // if set, the epilogue factor is alpha_scale * (*alpha_dev), read on the
+  // device after the preceding kernel on the stream has completed
+  const float* alpha_dev = nullptr;
+  float alpha_scale = 1.0f;
 };
 
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, const CUtensorMap& tmap_a,

@@ -163,6 +163,23 @@ petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* rep,
                                      void* workspace, size_t workspace_bytes,
                                      petit_stream_t stream);
 
+/* Same as petit_gemm_bf16_nvfp4, with the global scale g read from device
+ * memory: `global_scale_dev` points to one FP32 value (4-byte aligned) that
+ * the kernel reads after the preceding kernel on `stream` has completed, so a
+ * kernel earlier in the same stream or CUDA graph may compute it (for
+ * example from petit_absmax_bf16 output), and a captured graph picks up a new
+ * value on every replay without re-capture.  The pages leave g to a host
+ * float; this entry point is for serving steps built as CUDA graphs (Petit
+ * PyPI page, "Features": integration with serving stacks).  The value must be positive
+ * and finite; it is not checked on the device.
+ * Errors: as petit_gemm_bf16_nvfp4, and PETIT_ERR_INVALID_ARG for a null or
+ * misaligned global_scale_dev. */
+petit_status_t petit_gemm_bf16_nvfp4_dscale(const void* A, const uint8_t* rep,
+                                            const float* global_scale_dev, void* C,
+                                            int64_t m, int64_t n, int64_t k,
+                                            void* workspace, size_t workspace_bytes,
+                                            petit_stream_t stream);
+
 /* Same with repacked MXFP4 weights and E8M0 scales (no global scale). */
 petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,
                                      int64_t m, int64_t n, int64_t k,

@@ -239,3 +239,32 @@ def test_back_to_back_prefill_tiles(cuda_lib):
     for j, c in enumerate(outs):
         assert torch.equal(c, probs[j % 2][4]), f"launch {j}"
     assert all(p[3].status() == 0 for p in probs)
+
+
+def test_device_global_scale_in_graph(cuda_lib):
+    """The device-pointer global scale: same bits as the host-scale call, and
+    a captured CUDA graph picks up a new value on replay (g doubled -> every
+    BF16 output exactly doubled)."""
+    n, k, m = 1024, 2048, 16
+    w = synth.weights(n, k, seed=80)
+    g0 = float(quantize.nvfp4_global_scale(w.float().numpy()))
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4", g0)
+    a = synth.activations(m, k, seed=81).cuda()
+    ref = _gemm(cuda_lib, a, rep, n, "nvfp4", g0)
+    gdev = torch.tensor([g0], dtype=torch.float32, device="cuda")
+    ws = cuda_lib.Workspace()
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.gemm(a, rep, n, "nvfp4", gdev, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            cuda_lib.gemm(a, rep, n, "nvfp4", gdev, workspace=ws, out=out)
+        gdev.fill_(2.0 * g0)
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.float(), 2.0 * ref.float())
+    assert ws.status() == 0
+    assert_parity(ref, oracle_reference(a.cpu(), codes, scales, "nvfp4", g0), "device g")
