@@ -45,10 +45,8 @@ namespace {
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;     // tensor-memory owner and MMA issuer 0
 constexpr int kEpiWarp0 = 2;    // warps 2..5
-constexpr int kDeqWarp0 = 6;    // warps 6..13
-constexpr int kNumDeqWarps = 8;
+constexpr int kDeqWarp0 = 6;    // dequantiser warps 6 .. 6 + 4 * groups - 1
 constexpr int kDeqGroupWarps = 4;   // one dequantiser group: a warp per lane quarter
-constexpr int kMmaWarpX = 13;   // MMA issuer t >= 1 is warp 13 + t (warps 14, 15)
 constexpr int kMaxMmaThreads = 3;
 constexpr uint32_t kTmemCols = 512;
 
@@ -81,7 +79,10 @@ struct Cfg {
   // Three issuers (warps 1, 14, 15 on sub-partitions 1, 2, 3) keep the CTA
   // at 16 warps, four per sub-partition, so each thread may use 128 registers.
   static constexpr int kMmaThreads = BN <= 32 ? 3 : BN <= 128 ? 2 : 1;
-  static constexpr int kThreads = 32 * (14 + kMmaThreads - 1);
+  // dequantiser groups (four warps each) taking units round-robin
+  static constexpr int kDeqGroups = 2;
+  static constexpr int kMmaWarpX = kDeqWarp0 + kDeqGroupWarps * kDeqGroups - 1;  // issuer t>=1: +t
+  static constexpr int kThreads = 32 * (kMmaWarpX + kMmaThreads);
   static constexpr int kAColsPerUnit = KU * (kStageK / 2);     // BF16x2 columns
   // accumulator buffers per issuer: two when they fit beside three A-buffers
   // (the epilogue of one tile then overlaps the next tile's MMAs)
@@ -108,7 +109,8 @@ struct Cfg {
   static constexpr int kXStages0 = (kXBudget / kABytes) / kXMult * kXMult;
   static constexpr int kXStages = kXStages0 > 16 ? 16 / kXMult * kXMult : kXStages0;
   static constexpr int kRingBytes = 220 * 1024;
-  static constexpr int kWStages0 = (kRingBytes - kXStages * kABytes) / kWBytes / 2 * 2;
+  static constexpr int kWStages0 =
+      (kRingBytes - kXStages * kABytes) / kWBytes / kDeqGroups * kDeqGroups;
   static constexpr int kWStages = kWStages0 > 12 ? 12 : kWStages0;
   static constexpr int kNumA1 = (kNumA0 > 4 ? 4 : kNumA0) / kMmaThreads * kMmaThreads;
   static constexpr int kNumA = kNumA1 > kXStages ? kXStages / kMmaThreads * kMmaThreads : kNumA1;
@@ -120,8 +122,8 @@ struct Cfg {
   static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
                 "tensor memory");
   static_assert(kMmaThreads <= kMaxMmaThreads, "issuers");
-  static_assert(kWStages >= 2 && kXStages >= 2 && kWStages % 2 == 0, "pipeline depth");
-  static_assert(kXStages % kMmaThreads == 0 && (kMmaThreads == 1 || kXStages % 2 == 0) &&
+  static_assert(kWStages >= 2 && kXStages >= 2 && kWStages % kDeqGroups == 0, "pipeline depth");
+  static_assert(kXStages % kMmaThreads == 0 && (kMmaThreads == 1 || kXStages % kDeqGroups == 0) &&
                     kNumA % kMmaThreads == 0 && kNumA <= kXStages,
                 "fixed consumer per barrier");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -295,9 +297,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
                             p.timeout_ns, nullptr);
       }
     }
-  } else if (warp == kMmaWarp || warp > kMmaWarpX) {
+  } else if (warp == kMmaWarp || warp > C::kMmaWarpX) {
     // ------------------------------------------------------------ MMA issue
-    const int t = warp == kMmaWarp ? 0 : warp - kMmaWarpX;   // issues units i % kMmaThreads == t
+    const int t = warp == kMmaWarp ? 0 : warp - C::kMmaWarpX;   // issues units i % kMmaThreads == t
     if (lane == 0) {
       int64_t seg = 0;
       int st = 0, b = 0;
@@ -491,51 +493,47 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     }
   } else {
     // ---------------------------------------------------------- dequantise
-    // Two groups of four warps take alternate units; a warp decodes both
-    // 64-k halves of its 32 rows.  The two dequantiser warps of an SM
-    // sub-partition then work on different units, so one's barrier waits
-    // and round trips overlap the other's decode arithmetic.
+    // kDeqGroups groups of four warps take units round-robin; a warp decodes
+    // both 64-k halves of its 32 rows, one 32-k group pair at a time.  The
+    // dequantiser warps of an SM sub-partition then work on different
+    // units, so one's barrier waits and round trips overlap the others'
+    // decode arithmetic.
     const int grp = (warp - kDeqWarp0) / kDeqGroupWarps;
     const int q = warp & 3;         // tensor-memory lane quarter
     const int r = 32 * q + lane;    // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     int64_t i = 0;
-    int st = 0, b = 0, st2 = 0;   // st2: stage of unit i - kNumA
+    int owner = 0;                // unit i's group: i % kDeqGroups
+    int st = 0, b = 0, st2 = 0;   // st: weight stage of unit i; st2: activation stage of i - kNumA
     uint32_t ph = 0, ph2 = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
-      if ((i & 1) == grp) {
+      if (owner == grp) {
         if (!wait(&wfull[st], ph)) break;
         bool ok = true;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4 g[KU][2];
-          uint32_t sv[KU];
-#pragma unroll
-          for (int j = 0; j < KU; ++j) {
-            const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
-            g[j][0] = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
-            g[j][1] = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
-            if constexpr (FMT == kNVFP4)
-              sv[j] = *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
-            else
-              sv[j] = *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
+        for (int hj = 0; hj < 2 * KU; ++hj) {
+          const int h = hj / KU, j = hj % KU;
+          const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+          const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+          const uint4 g1 = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+          uint32_t o[2][16];
+          if constexpr (FMT == kNVFP4) {
+            const uint32_t sv =
+                *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
+            decode_group<FMT>(g0, sv & 0xFFFFu, o[0]);
+            decode_group<FMT>(g1, sv >> 16, o[1]);
+          } else {
+            const uint32_t sv =
+                *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
+            decode_group<FMT>(g0, sv & 0xFFu, o[0]);
+            decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
           }
-          uint32_t o[KU][2][16];
-#pragma unroll
-          for (int j = 0; j < KU; ++j) {
-            if constexpr (FMT == kNVFP4) {
-              decode_group<FMT>(g[j][0], sv[j] & 0xFFFFu, o[j][0]);
-              decode_group<FMT>(g[j][1], sv[j] >> 16, o[j][1]);
-            } else {
-              decode_group<FMT>(g[j][0], sv[j] & 0xFFu, o[j][0]);
-              decode_group<FMT>(g[j][1], (sv[j] >> 8) & 0xFFu, o[j][1]);
-            }
-          }
-          if (h == 1) {
+          if (hj == 2 * KU - 1) {
             // the decode consumed every byte this warp read: release the chunk
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
-          } else if (i >= C::kNumA) {
+          }
+          if (hj == 0 && i >= C::kNumA) {
             // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
             // and order the stores below after their operand reads
             if (!wait(&mdone[st2], ph2)) {
@@ -544,13 +542,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             }
             tc_fence_after();
           }
-#pragma unroll
-          for (int j = 0; j < KU; ++j) {
-            const uint32_t acol =
-                tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
-            tmem_st_x16(acol, o[j][0]);
-            tmem_st_x16(acol + 16, o[j][1]);
-          }
+          const uint32_t acol =
+              tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+          tmem_st_x16(acol, o[0]);
+          tmem_st_x16(acol + 16, o[1]);
         }
         if (!ok) break;
         tmem_wait_st();
@@ -558,6 +553,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       }
+      if (++owner == C::kDeqGroups) owner = 0;
       if (++st == C::kWStages) {
         st = 0;
         ph ^= 1u;
