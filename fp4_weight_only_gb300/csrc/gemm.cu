@@ -199,7 +199,26 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap_a);
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    // Weights are never written by the preceding kernel, and L2 is the
+    // device's point of coherence, so the first ring's worth of this CTA's
+    // weight chunks can be pulled into L2 before the grid dependency wait
+    // (while the previous kernel finishes); the copies after the wait then
+    // hit L2.
+    const int64_t tile0 = u0 / KS;
+    int64_t ku = u0 - tile0 * KS, nt = tile0 / p.m_tiles, mt = tile0 - nt * p.m_tiles;
+    for (int64_t u = u0; u < u1 && u < u0 + C::kWStages; ++u) {
+      bulk_prefetch_l2(p.rep + chunk_offset<FMT>(nt, ku * KU, KS * KU), C::kWBytes);
+      if (++ku == KS) {
+        ku = 0;
+        if (++mt == p.m_tiles) {
+          mt = 0;
+          ++nt;
+        }
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -109,6 +109,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   return p;
 }
 
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned address) of global
+// memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Contiguous global -> shared bulk copy completing on an mbarrier (bytes and
 // both addresses 16-byte multiples).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
