@@ -379,9 +379,10 @@ def run_ours(args, rank, world, local):
         return reps, gs
 
     def shape_table(fmt, reps, gs, m, seed0, outliers=0.0, burst_reps=10):
-        a = [synth.activations(m, k, seed=seed0 + i, device=dev, outlier_frac=outliers)
+        act = torch.float16 if fmt == "nvfp4_f16" else torch.bfloat16
+        a = [synth.activations(m, k, seed=seed0 + i, device=dev, outlier_frac=outliers).to(act)
              for i, (_, n, k) in enumerate(SHAPES)]
-        c = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for _, n, _ in SHAPES]
+        c = [torch.empty((m, n), dtype=act, device=dev) for _, n, _ in SHAPES]
 
         def fn(i, w):
             binding.gemm(a[i], reps[w][i], SHAPES[i][1], fmt, gs[i], workspace=ws, out=c[i])
@@ -395,7 +396,7 @@ def run_ours(args, rank, world, local):
         out = {}
         for i, (name, n, k) in enumerate(SHAPES):
             t = ms[i] * 1e-3
-            b = algo_bytes(m, n, k, 16 if fmt == "nvfp4" else 32)
+            b = algo_bytes(m, n, k, 32 if fmt == "mxfp4" else 16)
             tf = 2 * m * n * k / t / 1e12
             out[name] = {"us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 2),
                          "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3),
@@ -404,6 +405,7 @@ def run_ours(args, rank, world, local):
         return out
 
     prefill = None
+    fp16_decode = None
     mxfp4 = None
     m_sweep = None
     cublas = None
@@ -416,6 +418,10 @@ def run_ours(args, rank, world, local):
         reps_mx, gs_mx = prepared("mxfp4", 600, False)
         mxfp4 = {f"m={m}": shape_table("mxfp4", reps_mx, gs_mx, m, 700 + m) for m in (1, 4, 8, 16, 256)}
         del reps_mx
+        # FP16-activation variant, NVFP4 decode m = 16
+        reps_h, gs_h = prepared("nvfp4_f16", 650, False)
+        fp16_decode = shape_table("nvfp4_f16", reps_h, gs_h, M_DECODE, 660)
+        del reps_h
         # NVFP4 m sweep at n = k = 8192 (two weight copies), and m = n = k = 4096
         m_sweep = {}
         for (n, k, ms_list) in ((8192, 8192, (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)), (4096, 4096, (4096,))):
@@ -486,7 +492,8 @@ def run_ours(args, rank, world, local):
             "tflops": round(world * step_flops * args.steps / (elapsed_max * 1e-3) / 1e12, 2),
             "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
-            "prefill_m256": prefill, "mxfp4_decode": mxfp4, "m_sweep": m_sweep,
+            "prefill_m256": prefill, "mxfp4_decode": mxfp4, "fp16_decode_m16": fp16_decode,
+            "m_sweep": m_sweep,
             "cublas_bf16_context": cublas,
         }
         print(json.dumps(out), flush=True)

@@ -16,7 +16,8 @@ from . import build as _build
 
 PETIT_FMT_NVFP4 = 0
 PETIT_FMT_MXFP4 = 1
-FORMATS = {"nvfp4": PETIT_FMT_NVFP4, "mxfp4": PETIT_FMT_MXFP4}
+PETIT_FMT_NVFP4_F16 = 2
+FORMATS = {"nvfp4": PETIT_FMT_NVFP4, "mxfp4": PETIT_FMT_MXFP4, "nvfp4_f16": PETIT_FMT_NVFP4_F16}
 
 STATUS = {
     0: "PETIT_OK",
@@ -48,6 +49,10 @@ SIGNATURES = {
     "petit_quantize_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
     "petit_repack_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
     "petit_repack_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_repack_nvfp4_f16": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_dequant_f16": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p]),
+    "petit_gemm_f16_nvfp4": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
+                                            _c_p, _c_sz, _c_p]),
     "petit_dequant_bf16": (ctypes.c_int, [_c_p, ctypes.c_int, _c_p, _c_i64, _c_i64, _c_p]),
     "petit_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
                                              _c_p, _c_sz, _c_p]),
@@ -147,13 +152,19 @@ def repack(w_packed, scales, fmt="nvfp4"):
     L = load()
     out = torch.empty(max(L.petit_repacked_bytes(n, k, FORMATS[fmt]), 1), dtype=torch.uint8,
                       device=w_packed.device)
-    fn = L.petit_repack_nvfp4 if fmt == "nvfp4" else L.petit_repack_mxfp4
+    fn = {"nvfp4": L.petit_repack_nvfp4, "mxfp4": L.petit_repack_mxfp4,
+          "nvfp4_f16": L.petit_repack_nvfp4_f16}[fmt]
     _check(fn(_ptr(w_packed), _ptr(scales), _ptr(out), n, k, _stream()), "repack_" + fmt)
     return out
 
 
 def dequant(rep, n, k, fmt="nvfp4"):
-    """Repacked weights -> BF16 Wq [n, k] (test hook; bit-exact)."""
+    """Repacked weights -> Wq [n, k] (test hook; bit-exact): BF16, or FP16 for
+    the "nvfp4_f16" layout."""
+    if fmt == "nvfp4_f16":
+        out = torch.empty((n, k), dtype=torch.float16, device=rep.device)
+        _check(load().petit_dequant_f16(_ptr(rep), _ptr(out), n, k, _stream()), "dequant_f16")
+        return out
     out = torch.empty((n, k), dtype=torch.bfloat16, device=rep.device)
     _check(load().petit_dequant_bf16(_ptr(rep), FORMATS[fmt], _ptr(out), n, k, _stream()), "dequant")
     return out
@@ -183,17 +194,22 @@ class Workspace:
 def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
     """C[m, n] = g * A @ dequant(W)^T in BF16 (FP32 accumulation).  For NVFP4,
     `global_scale` is a float or a one-element FP32 CUDA tensor (read by the
-    kernel, so a CUDA graph picks up a changed value on replay)."""
-    _need(A, torch.bfloat16, "A")
+    kernel, so a CUDA graph picks up a changed value on replay).  With the
+    "nvfp4_f16" layout, A and C are FP16."""
+    act = torch.float16 if fmt == "nvfp4_f16" else torch.bfloat16
+    _need(A, act, "A")
     m, k = A.shape
     ws = workspace or Workspace(A.device)
     need = workspace_bytes(m, n, k, fmt)
     if need == 0:
         raise PetitError(2, "gemm workspace size")
     buf = ws.ensure(need)
-    C = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=A.device)
+    C = out if out is not None else torch.empty((m, n), dtype=act, device=A.device)
     L = load()
-    if fmt == "nvfp4" and isinstance(global_scale, torch.Tensor):
+    if fmt == "nvfp4_f16":
+        st = L.petit_gemm_f16_nvfp4(_ptr(A), _ptr(rep), ctypes.c_float(global_scale), _ptr(C),
+                                    m, n, k, _ptr(buf), buf.numel(), _stream())
+    elif fmt == "nvfp4" and isinstance(global_scale, torch.Tensor):
         _need(global_scale, torch.float32, "global_scale")
         st = L.petit_gemm_bf16_nvfp4_dscale(_ptr(A), _ptr(rep), _ptr(global_scale), _ptr(C),
                                             m, n, k, _ptr(buf), buf.numel(), _stream())
@@ -218,7 +234,7 @@ class FP4Weight:
     def __init__(self, W, fmt="nvfp4", global_scale=None):
         n, k = W.shape
         self.n, self.k, self.fmt = n, k, fmt
-        if fmt == "nvfp4":
+        if fmt in ("nvfp4", "nvfp4_f16"):
             if global_scale is None:
                 global_scale = 1.0
             elif global_scale == "amax":
@@ -226,7 +242,7 @@ class FP4Weight:
             self.global_scale = float(global_scale)
         else:
             self.global_scale = 1.0
-        w_packed, scales = quantize(W, fmt, self.global_scale)
+        w_packed, scales = quantize(W, "mxfp4" if fmt == "mxfp4" else "nvfp4", self.global_scale)
         self.rep = repack(w_packed, scales, fmt)
 
     def __call__(self, A, workspace=None, out=None):

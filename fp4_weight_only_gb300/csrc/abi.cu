@@ -12,6 +12,7 @@ namespace {
 
 using petit::kMXFP4;
 using petit::kNVFP4;
+using petit::kNVFP4F16;
 
 constexpr int64_t kMaxDim = int64_t(1) << 24;
 constexpr uint64_t kGemmTimeoutNs = 2000000000ull;  // no legitimate wait lasts 2 s
@@ -79,14 +80,15 @@ EncodeTiledFn encode_fn() {
 // slabs of 64 k for bn rows (128-byte swizzle, zero fill for rows >= m), i.e.
 // a whole pipeline unit's activations in one request.
 petit_status_t encode_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t k, int bn,
-                            int ku) {
+                            int ku, bool f16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return PETIT_ERR_CUDA;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(k / 64)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * 2, 128};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bn), static_cast<cuuint32_t>(2 * ku)};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), dims, strides,
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(A), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PETIT_OK : PETIT_ERR_CUDA;
@@ -114,7 +116,8 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
+  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku, fmt == kNVFP4F16))
+    return st;
   petit::GemmArgs args{A, rep, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
   if (alpha_dev) {
     args.alpha_dev = alpha_dev;
@@ -146,14 +149,14 @@ const char* petit_status_string(petit_status_t s) {
 size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt) {
   if (n < 0 || k < 0) return 0;
   const size_t nk = static_cast<size_t>(n) * static_cast<size_t>(k);
-  if (fmt == PETIT_FMT_NVFP4) return nk / 2 + nk / 16;
+  if (fmt == PETIT_FMT_NVFP4 || fmt == PETIT_FMT_NVFP4_F16) return nk / 2 + nk / 16;
   if (fmt == PETIT_FMT_MXFP4) return nk / 2 + nk / 32;
   return 0;
 }
 
 size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt) {
   if (m < 1 || m > kMaxDim || check_tiled_shape(n, k) != PETIT_OK) return 0;
-  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return 0;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4 && fmt != PETIT_FMT_NVFP4_F16) return 0;
   int sms = 0;
   if (current_device(&sms) != PETIT_OK) return 0;
   return petit::plan_gemm(m, n, k, fmt, sms).ws.total;
@@ -208,6 +211,12 @@ petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3
   return repack_common(kNVFP4, w_packed, s_e4m3, rep_out, n, k, stream);
 }
 
+petit_status_t petit_repack_nvfp4_f16(const uint8_t* w_packed, const uint8_t* s_e4m3,
+                                      uint8_t* rep_out, int64_t n, int64_t k,
+                                      petit_stream_t stream) {
+  return repack_common(kNVFP4F16, w_packed, s_e4m3, rep_out, n, k, stream);
+}
+
 petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0, uint8_t* rep_out,
                                   int64_t n, int64_t k, petit_stream_t stream) {
   return repack_common(kMXFP4, w_packed, s_e8m0, rep_out, n, k, stream);
@@ -222,6 +231,25 @@ petit_status_t petit_dequant_bf16(const uint8_t* rep, int fmt, void* W_out, int6
   if (petit_status_t st = current_device(nullptr)) return st;
   return from_cuda(
       petit::launch_dequant(fmt, rep, W_out, n, k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+petit_status_t petit_dequant_f16(const uint8_t* rep, void* W_out, int64_t n, int64_t k,
+                                 petit_stream_t stream) {
+  if (!rep || !W_out) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (!aligned16(rep) || !aligned16(W_out)) return PETIT_ERR_MISALIGNED;
+  if (petit_status_t st = current_device(nullptr)) return st;
+  return from_cuda(petit::launch_dequant(kNVFP4F16, rep, W_out, n, k,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+petit_status_t petit_gemm_f16_nvfp4(const void* A, const uint8_t* rep, float global_scale, void* C,
+                                    int64_t m, int64_t n, int64_t k, void* workspace,
+                                    size_t workspace_bytes, petit_stream_t stream) {
+  if (!(global_scale > 0.0f) || global_scale > 1.0e36f) return PETIT_ERR_INVALID_ARG;
+  // the FP16 register decode yields Wq * 2^-7; the epilogue restores it with g
+  return gemm_common(kNVFP4F16, A, rep, global_scale * 128.0f, C, m, n, k, workspace,
+                     workspace_bytes, stream);
 }
 
 petit_status_t petit_gemm_bf16_nvfp4(const void* A, const uint8_t* rep, float global_scale,

@@ -26,7 +26,9 @@ constexpr int kStageK = 128;  // k elements per repacked chunk / pipeline stage
 constexpr int kWChunkBytes = kTileN * kStageK / 2;  // 8192
 constexpr int kGroupsPerRow = kStageK / 32;         // 16-byte groups per row per chunk
 
-enum : int { kNVFP4 = 0, kMXFP4 = 1 };
+// kNVFP4F16: NVFP4 codes and scales packed for the FP16-activation GEMM
+// (same chunk layout and sizes, FP16 bit positions; see pack_word_f16)
+enum : int { kNVFP4 = 0, kMXFP4 = 1, kNVFP4F16 = 2 };
 
 template <int FMT>
 struct FmtTraits;
@@ -37,6 +39,8 @@ struct FmtTraits<kNVFP4> {
   static constexpr int kScaleBytesPerHalf = 4;               // 64 k / 16
   static constexpr int kChunkBytes = kWChunkBytes + kSChunkBytes;  // 9216
 };
+template <>
+struct FmtTraits<kNVFP4F16> : FmtTraits<kNVFP4> {};
 template <>
 struct FmtTraits<kMXFP4> {
   static constexpr int kBlock = 32;
@@ -84,6 +88,26 @@ __host__ __device__ inline uint32_t pack_word(const uint32_t (&c)[8]) {
   return q;
 }
 
+// FP16 variant.  FP16 has its exponent's two low bits at 11 and 10 and its top
+// mantissa bit at 9, so sign/e1/e0/m on bits 15/11/10/9 give the FP16 number
+// value(code) * 2^-14 exactly (code 0.5 -> the FP16 subnormal 2^-15).  The
+// 8 codes of a word sit where two shifted copies and two two-part merges
+// put them (decode_word_raw_f16); code bits (m, e0, e1, s) at:
+//   c0:  5  6  7 11    c1: 21 22 23 27    (decode: (q << 4) & M16)
+//   c2:  2  3  4  8    c3: 18 19 20 24    (decode: (q << 7) & M16)
+//   c4: 30 10  0 15    c5: 14 26 16 31    (decode: q & K | rot(q, 11) & K')
+//   c6:  9 28 29  1    c7: 25 12 13 17    (decode: q & K | rot(q, 14) & K')
+// with M16 = 0x8E008E00 selecting FP16 bits {15, 11, 10, 9} of both halves.
+__host__ __device__ inline uint32_t pack_word_f16(const uint32_t (&c)[8]) {
+  // bit positions of (m, e0, e1, s) for each code
+  constexpr int pos[8][4] = {{5, 6, 7, 11},   {21, 22, 23, 27}, {2, 3, 4, 8},     {18, 19, 20, 24},
+                             {30, 10, 0, 15}, {14, 26, 16, 31}, {9, 28, 29, 1},   {25, 12, 13, 17}};
+  uint32_t q = 0;
+  for (int i = 0; i < 8; ++i)
+    for (int b = 0; b < 4; ++b) q |= ((c[i] >> b) & 1u) << pos[i][b];
+  return q;
+}
+
 // ---------------------------------------------------------------- decode
 // Four BF16x2 words value(c_i) * 2^-126 for the pairs (c0,c1) .. (c6,c7).
 __device__ __forceinline__ void decode_word_raw(uint32_t q, uint32_t (&p)[4]) {
@@ -92,6 +116,34 @@ __device__ __forceinline__ void decode_word_raw(uint32_t q, uint32_t (&p)[4]) {
   p[1] = (q << 3) & M;
   p[2] = (q << 6) & M;
   p[3] = ((q >> 6) & 0x01800180u) | ((q >> 4) & 0x00400040u) | ((q << 4) & 0x80008000u);
+}
+
+// Four FP16x2 words value(c_i) * 2^-14 for the pairs (c0,c1) .. (c6,c7) of a
+// word packed by pack_word_f16.
+__device__ __forceinline__ void decode_word_raw_f16(uint32_t q, uint32_t (&p)[4]) {
+  constexpr uint32_t M16 = 0x8E008E00u;
+  p[0] = (q << 4) & M16;
+  p[1] = (q << 7) & M16;
+  p[2] = (q & 0x84008400u) | (__funnelshift_l(q, q, 11) & 0x0A000A00u);
+  p[3] = (q & 0x02000200u) | (__funnelshift_l(q, q, 14) & 0x8C008C00u);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+constexpr uint32_t kF16x2_2p7 = 0x58005800u;  // 2^7 in both halves
+
+// Two E4M3 bytes -> FP16x2 splats of scale * 2^7 (exact: E4M3 -> FP16 is
+// exact and 448 * 2^7 < 65504).
+__device__ __forceinline__ void nv_scale_splats_f16(uint32_t v, uint32_t& s0, uint32_t& s1) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(v & 0xFFFFu)));
+  h2 = hmul2(h2, kF16x2_2p7);
+  s0 = __byte_perm(h2, 0, 0x1010);
+  s1 = __byte_perm(h2, 0, 0x3232);
 }
 
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
@@ -131,11 +183,24 @@ constexpr uint32_t kBf16x2_2p8 = 0x43804380u;    // 2^8 in both halves
 // Decode one 16-byte group (32 codes) into 16 BF16x2 words: out[j] holds k =
 // 2j (low half) and 2j+1 (high half).  NVFP4: sc holds the two E4M3 bytes of
 // the group (k 0-15, 16-31); result = Wq * 2^-8.  MXFP4: sc holds the E8M0
-// byte; result = Wq.
+// byte; result = Wq.  NVFP4F16: FP16x2 words, result = Wq * 2^-7.
 template <int FMT>
 __device__ __forceinline__ void decode_group(const uint4& g, uint32_t sc, uint32_t (&out)[16]) {
   const uint32_t w[4] = {g.x, g.y, g.z, g.w};
-  if constexpr (FMT == kNVFP4) {
+  if constexpr (FMT == kNVFP4F16) {
+    // FP16: value * 2^-14 times (scale * 2^7) = Wq * 2^-7, exact (the
+    // smallest product, 2^-17, is an FP16 subnormal with room to spare)
+    uint32_t s0, s1;
+    nv_scale_splats_f16(sc, s0, s1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t p[4];
+      decode_word_raw_f16(w[i], p);
+      const uint32_t s = i < 2 ? s0 : s1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) out[4 * i + j] = hmul2(p[j], s);
+    }
+  } else if constexpr (FMT == kNVFP4) {
     uint32_t s0, s1;
     nv_scale_splats(sc, s0, s1);
 #pragma unroll

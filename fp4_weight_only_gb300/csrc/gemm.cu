@@ -34,6 +34,7 @@
 // * Every wait is bounded; a wait that runs out records a timeout in the
 //   workspace status word and the CTA shuts down cleanly.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fp4_layout.cuh"
 #include "internal.h"
@@ -52,7 +53,7 @@ constexpr uint32_t kTmemCols = 512;
 
 struct Params {
   const uint8_t* rep;
-  __nv_bfloat16* c;
+  uint16_t* c;              // BF16 (or FP16 for the FP16 layout) [m][n]
   float* partials;
   uint32_t* counters;
   uint32_t* status;
@@ -116,7 +117,8 @@ struct Cfg {
   static constexpr int kNumA = kNumA1 > kXStages ? kXStages / kMmaThreads * kMmaThreads : kNumA1;
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
   static constexpr int kSmemBytes = 1024 + kXStages * kABytes + kWStages * kWBytes + 1024;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+  static constexpr uint32_t kIdesc =
+      FMT == kNVFP4F16 ? idesc_f16_f32(128, BN) : idesc_bf16_f32(128, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
@@ -128,6 +130,13 @@ struct Cfg {
                 "fixed consumer per barrier");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
+
+// Output element bits: BF16, or FP16 for the FP16-activation layout (RNE).
+template <int FMT>
+__device__ __forceinline__ uint16_t out_bits(float x) {
+  if constexpr (FMT == kNVFP4F16) return __half_as_ushort(__float2half_rn(x));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
 
 // CTA that owns stream-K unit u when U units are split over P CTAs with
 // CTA c covering [floor(c U / P), floor((c+1) U / P)).
@@ -438,7 +447,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           for (int j = 0; j < 16; ++j) {
             const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
             if (mrow < p.m)
-              p.c[mrow * p.n + ncol] = __float2bfloat16_rn(alpha * __uint_as_float(v[j]));
+              p.c[mrow * p.n + ncol] = out_bits<FMT>(alpha * __uint_as_float(v[j]));
           }
         } else {
 #pragma unroll
@@ -502,7 +511,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-              if (mrow < p.m) p.c[mrow * p.n + ncol] = __float2bfloat16_rn(alpha * acc[j]);
+              if (mrow < p.m) p.c[mrow * p.n + ncol] = out_bits<FMT>(alpha * acc[j]);
             }
           }
         }
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
           const uint4 g1 = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
           uint32_t o[2][16];
-          if constexpr (FMT == kNVFP4) {
+          if constexpr (FMT == kNVFP4 || FMT == kNVFP4F16) {
             const uint32_t sv =
                 *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
             decode_group<FMT>(g0, sv & 0xFFFFu, o[0]);
@@ -672,7 +681,7 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
                         cudaStream_t stream) {
   Params prm{};
   prm.rep = a.rep;
-  prm.c = static_cast<__nv_bfloat16*>(a.C);
+  prm.c = static_cast<uint16_t*>(a.C);
   prm.partials = reinterpret_cast<float*>(a.workspace + pl.ws.partials_off);
   prm.counters = reinterpret_cast<uint32_t*>(a.workspace + pl.ws.counters_off);
   prm.status = reinterpret_cast<uint32_t*>(a.workspace);
@@ -687,6 +696,7 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   prm.alpha_scale = a.alpha_scale;
   prm.timeout_ns = a.timeout_ns;
   if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream);
+  if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream);
   return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream);
 }
 

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
       uint32_t c[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) c[j] = (iw[w] >> (4 * j)) & 0xFu;
-      ow[w] = pack_word(c);
+      ow[w] = FMT == kNVFP4F16 ? pack_word_f16(c) : pack_word(c);
     }
     *reinterpret_cast<uint4*>(dst + static_cast<size_t>(i) * 16) =
         make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
 
 // ------------------------------------------------------------- dequant hook
 // One thread per (chunk, group, row): decodes 32 codes with the GEMM's decode
-// and writes Wq = code * scale as BF16 [n][k].
+// and writes Wq = code * scale as BF16 [n][k] (FP16 for the FP16 layout).
 template <int FMT>
-__global__ void dequant_kernel(const uint8_t* __restrict__ rep, __nv_bfloat16* __restrict__ out,
+__global__ void dequant_kernel(const uint8_t* __restrict__ rep, uint16_t* __restrict__ out,
                                int64_t n, int64_t k) {
   using T = FmtTraits<FMT>;
   const int64_t stages = k / kStageK;
@@ -213,7 +213,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ rep, __nv_bfloat16* _
     const uint8_t* cbase = rep + chunk * T::kChunkBytes;
     const uint4 grp = *reinterpret_cast<const uint4*>(cbase + within * 16);
     uint32_t sc;
-    if constexpr (FMT == kNVFP4) {
+    if constexpr (FMT == kNVFP4 || FMT == kNVFP4F16) {
       sc = *reinterpret_cast<const uint16_t*>(cbase + kWChunkBytes + (h * 128 + r) * 4 + (g & 1) * 2);
     } else {
       sc = cbase[kWChunkBytes + (h * 128 + r) * 2 + (g & 1)];
@@ -223,6 +223,9 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ rep, __nv_bfloat16* _
     if constexpr (FMT == kNVFP4) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) o[j] = bmul2(o[j], kBf16x2_2p8);  // undo 2^-8, exact
+    } else if constexpr (FMT == kNVFP4F16) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] = hmul2(o[j], kF16x2_2p7);  // undo 2^-7, exact
     }
     uint4* dst = reinterpret_cast<uint4*>(out + (t * kTileN + r) * k + s * kStageK + g * 32);
 #pragma unroll
@@ -272,6 +275,8 @@ cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t
   const dim3 grid(static_cast<unsigned>(k / kStageK), static_cast<unsigned>(n / kTileN));
   if (fmt == kNVFP4)
     repack_kernel<kNVFP4><<<grid, kThreads, 0, stream>>>(wp, sp, out, k);
+  else if (fmt == kNVFP4F16)
+    repack_kernel<kNVFP4F16><<<grid, kThreads, 0, stream>>>(wp, sp, out, k);
   else
     repack_kernel<kMXFP4><<<grid, kThreads, 0, stream>>>(wp, sp, out, k);
   return cudaGetLastError();
@@ -280,9 +285,11 @@ cudaError_t launch_repack(int fmt, const uint8_t* wp, const uint8_t* sp, uint8_t
 cudaError_t launch_dequant(int fmt, const uint8_t* rep, void* out, int64_t n, int64_t k,
                            cudaStream_t stream) {
   const int64_t total = (n / kTileN) * (k / kStageK) * (kTileN * kGroupsPerRow);
-  auto* o = static_cast<__nv_bfloat16*>(out);
+  auto* o = static_cast<uint16_t*>(out);
   if (fmt == kNVFP4)
     dequant_kernel<kNVFP4><<<grid_for(total), kThreads, 0, stream>>>(rep, o, n, k);
+  else if (fmt == kNVFP4F16)
+    dequant_kernel<kNVFP4F16><<<grid_for(total), kThreads, 0, stream>>>(rep, o, n, k);
   else
     dequant_kernel<kMXFP4><<<grid_for(total), kThreads, 0, stream>>>(rep, o, n, k);
   return cudaGetLastError();

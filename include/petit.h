@@ -61,8 +61,9 @@ typedef enum petit_status {
 } petit_status_t;
 
 typedef enum petit_format {
-  PETIT_FMT_NVFP4 = 0, /* E2M1 + E4M3 per 16 + FP32 global scale */
-  PETIT_FMT_MXFP4 = 1  /* E2M1 + E8M0 per 32 */
+  PETIT_FMT_NVFP4 = 0,     /* E2M1 + E4M3 per 16 + FP32 global scale */
+  PETIT_FMT_MXFP4 = 1,     /* E2M1 + E8M0 per 32 */
+  PETIT_FMT_NVFP4_F16 = 2  /* NVFP4 repacked for FP16 activations */
 } petit_format_t;
 
 /* Version of the repacked weight/scale order.  Stored repacked weights are
@@ -133,6 +134,13 @@ petit_status_t petit_repack_nvfp4(const uint8_t* w_packed, const uint8_t* s_e4m3
                                   uint8_t* rep_out, int64_t n, int64_t k,
                                   petit_stream_t stream);
 
+/* Same as petit_repack_nvfp4, with the codes at the bit positions of the
+ * FP16 decode used by petit_gemm_f16_nvfp4; output of
+ * petit_repacked_bytes(n, k, PETIT_FMT_NVFP4_F16) bytes. */
+petit_status_t petit_repack_nvfp4_f16(const uint8_t* w_packed, const uint8_t* s_e4m3,
+                                      uint8_t* rep_out, int64_t n, int64_t k,
+                                      petit_stream_t stream);
+
 /* Same as petit_repack_nvfp4 for MXFP4 scales s_e8m0 [n][k/32] (code 0xFF is
  * not a number and must not occur). */
 petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0,
@@ -146,6 +154,12 @@ petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0
  * aid in "FP4 GEMM on Rubin/Blackwell with CUTLASS", section 7.) */
 petit_status_t petit_dequant_bf16(const uint8_t* rep, int fmt, void* W_out,
                                   int64_t n, int64_t k, petit_stream_t stream);
+
+/* Test hook for the FP16 layout: repacked NVFP4 (from petit_repack_nvfp4_f16)
+ * -> FP16 Wq [n][k] (device), through the FP16 register decode, bit-exact.
+ * n % 128 == 0, k % 128 == 0. */
+petit_status_t petit_dequant_f16(const uint8_t* rep, void* W_out, int64_t n, int64_t k,
+                                 petit_stream_t stream);
 
 /* --------------------------------------------------------------- the GEMM */
 
@@ -179,6 +193,19 @@ petit_status_t petit_gemm_bf16_nvfp4_dscale(const void* A, const uint8_t* rep,
                                             int64_t m, int64_t n, int64_t k,
                                             void* workspace, size_t workspace_bytes,
                                             petit_stream_t stream);
+
+/* FP16-activation variant (Petit blog, "Introduction": FP16/BF16 activations
+ * with FP4 weights): C[m][n] FP16 = g * A[m][k] (FP16) * Wq[n][k]^T, FP32
+ * accumulation, FP16 round-to-nearest-even output.  `rep` comes from
+ * petit_repack_nvfp4_f16 (the same codes and E4M3 scales as the BF16 path,
+ * packed at FP16 bit positions).  Code x E4M3 scale is exact in FP16 for
+ * every code and scale, so the dequantised operand equals Wq.  Arguments,
+ * workspace (petit_gemm_workspace_bytes(m, n, k, PETIT_FMT_NVFP4_F16)) and
+ * errors as petit_gemm_bf16_nvfp4; A and C are FP16 [m][k] and [m][n]. */
+petit_status_t petit_gemm_f16_nvfp4(const void* A, const uint8_t* rep, float global_scale,
+                                    void* C, int64_t m, int64_t n, int64_t k,
+                                    void* workspace, size_t workspace_bytes,
+                                    petit_stream_t stream);
 
 /* Same with repacked MXFP4 weights and E8M0 scales (no global scale). */
 petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,

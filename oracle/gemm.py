@@ -55,6 +55,17 @@ def dequantize_bf16_bits(codes, scales, fmt):
     return bits
 
 
+def dequantize_f16_bits(codes, scales):
+    """IEEE binary16 bit patterns of the NVFP4 :func:`dequantize` (the FP16-
+    activation variant's operand, Petit blog "Introduction": FP16/BF16
+    activations); raises if any value is inexact in binary16."""
+    wq = dequantize(codes, scales, "nvfp4")
+    h = wq.astype(np.float16)
+    if not np.all(h.astype(np.float64) == wq):
+        raise ArithmeticError("dequantised weight not exactly representable in FP16")
+    return h.view(np.uint16)
+
+
 def gemm(a, wq, global_scale=1.0):
     """C = g * A . Wq^T in float64.  ``a`` [m, k], ``wq`` [n, k]."""
     a64 = np.asarray(a, dtype=np.float64)

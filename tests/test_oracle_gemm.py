@@ -67,3 +67,19 @@ def test_gemm_special_cases():
     rows = np.array([3, 11, 23])
     np.testing.assert_array_equal(gemm.gemm_rows(a, codes, sc, "nvfp4", 1.0, rows),
                                   gemm.gemm(a, wq, 1.0)[:, rows])
+
+
+def test_f16_dequant_bits_exact_and_pinned():
+    """Every E2M1 code times every positive finite E4M3 scale is exact in
+    binary16; spot values checked against their hand-computed bit patterns."""
+    codes = np.tile(np.arange(16, dtype=np.uint8), 126 * 16)[: 126 * 16 * 16].reshape(126 * 16, 16)
+    scales = np.repeat(np.arange(1, 127, dtype=np.uint8), 16).reshape(126 * 16, 1)
+    bits = gemm.dequantize_f16_bits(codes, scales)
+    wq = gemm.dequantize(codes, scales, "nvfp4")
+    np.testing.assert_array_equal(bits.view(np.float16).astype(np.float64), wq)
+    # code 0x1 (0.5) x scale 0x01 (2^-9) = 2^-10 -> binary16 0x1400;
+    # code 0xF (-6) x scale 0x7E (448) = -2688 -> 0xE940; code 0x8 (-0) -> 0x8000
+    c = np.array([[0x1, 0xF, 0x8] + [0] * 13], dtype=np.uint8)
+    for sc, idx, want in [(0x01, 0, 0x1400), (0x7E, 1, 0xE940), (0x30, 2, 0x8000)]:
+        b = gemm.dequantize_f16_bits(c, np.array([[sc]], dtype=np.uint8))
+        assert int(b[0, idx]) == want, (sc, idx, hex(int(b[0, idx])))
