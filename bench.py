@@ -409,6 +409,7 @@ def run_ours(args, rank, world, local):
     mxfp4 = None
     m_sweep = None
     cublas = None
+    moe = None
     if not args.no_prefill:
         # NVFP4 prefill: m = 256, 0.1 % N(0,20) activation outliers, g = amax/(6*448)
         reps_g, gs_g = prepared("nvfp4", 500, True)
@@ -448,6 +449,37 @@ def run_ours(args, rank, world, local):
                     else "tensor",
                     "frac_roofline": round(roof_t / t, 3)}
             del f0, r2
+        # MoE grouped GEMM: 8 experts, top-2, Mixtral-8x7B-like gate_up
+        # (n = 28672, k = 4096), MXFP4, seeded Zipf-like routing
+        moe = {}
+        E, n_e, k_e = 8, 28672, 4096
+        ew = []
+        for c in (0, 1):
+            reps_e = []
+            for e in range(E):
+                w = synth.weights(n_e, k_e, seed=1000 + 10 * c + e, device=dev)
+                reps_e.append(binding.FP4Weight(w, "mxfp4").rep)
+                del w
+            ew.append(torch.cat(reps_e))
+            del reps_e
+        for tokens in (16, 256):
+            off = synth.moe_expert_offsets(tokens, E, 2, seed=tokens)
+            a = synth.activations(off[-1], k_e, seed=1100 + tokens, device=dev)
+            cm = torch.empty((off[-1], n_e), dtype=torch.bfloat16, device=dev)
+
+            def fn(w, a=a, cm=cm, off=off):
+                binding.moe_gemm(a, ew[w], off, n_e, "mxfp4", workspace=ws, out=cm)
+            fn(0); fn(1)
+            torch.cuda.synchronize()
+            t = float(shape_durations([[lambda: fn(0), lambda: fn(1)]], stream, 10)[0]) * 1e-3
+            active = sum(1 for e in range(E) if off[e + 1] > off[e])
+            b = active * n_e * k_e * 17 // 32 + 2 * off[-1] * (k_e + n_e)
+            tf = 2 * off[-1] * n_e * k_e / t / 1e12
+            moe[f"tokens={tokens} top2 rows={off[-1]}"] = {
+                "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 1),
+                "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3), "active_experts": active,
+                "expert_rows": [off[e + 1] - off[e] for e in range(E)]}
+        del ew
         # context row: cuBLAS BF16 dense GEMM on the same shapes (BF16 weights are
         # 3.6x the NVFP4 bytes; two copies alternate so they come from HBM too)
         cublas = {}
@@ -494,7 +526,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
             "prefill_m256": prefill, "mxfp4_decode": mxfp4, "fp16_decode_m16": fp16_decode,
             "m_sweep": m_sweep,
-            "cublas_bf16_context": cublas,
+            "moe_mxfp4_gate_up": moe, "cublas_bf16_context": cublas,
         }
         print(json.dumps(out), flush=True)
 

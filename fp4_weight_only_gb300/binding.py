@@ -62,6 +62,11 @@ SIGNATURES = {
                                                     _c_p, _c_sz, _c_p]),
     "petit_gemm_bf16_nvfp4_noalloc": (ctypes.c_int, [_c_p, _c_p, ctypes.c_float, _c_p, _c_i64, _c_i64, _c_i64,
                                                      _c_p]),
+    "petit_moe_workspace_bytes": (_c_sz, [_c_p, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "petit_moe_gemm_bf16_mxfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_i64, _c_p,
+                                                 _c_sz, _c_p]),
+    "petit_moe_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_p, _c_sz, _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
 }
@@ -220,6 +225,35 @@ def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
         st = L.petit_gemm_bf16_mxfp4(_ptr(A), _ptr(rep), _ptr(C), m, n, k, _ptr(buf), buf.numel(),
                                      _stream())
     _check(st, "gemm_" + fmt)
+    return C
+
+
+def moe_gemm(A, rep, expert_offsets, n, fmt="mxfp4", global_scales=None, workspace=None, out=None):
+    """Grouped GEMM of an MoE layer: rows [off[e], off[e+1]) of A (BF16,
+    grouped by expert) times expert e's weights; `rep` holds the experts'
+    repacked weights back to back; `expert_offsets` is a host sequence of
+    E + 1 ints; `global_scales` (NVFP4) a host sequence of E floats."""
+    _need(A, torch.bfloat16, "A")
+    T, k = A.shape
+    off = (ctypes.c_int64 * len(expert_offsets))(*[int(x) for x in expert_offsets])
+    E = len(expert_offsets) - 1
+    if int(off[E]) != T:
+        raise ValueError("expert_offsets[-1] must equal A.shape[0]")
+    L = load()
+    ws = workspace or Workspace(A.device)
+    need = int(L.petit_moe_workspace_bytes(off, E, n, k, FORMATS[fmt]))
+    if need == 0 and T > 0:
+        raise PetitError(2, "moe workspace size")
+    buf = ws.ensure(max(need, 256))
+    C = out if out is not None else torch.empty((T, n), dtype=torch.bfloat16, device=A.device)
+    if fmt == "mxfp4":
+        st = L.petit_moe_gemm_bf16_mxfp4(_ptr(A), _ptr(rep), off, E, _ptr(C), n, k, _ptr(buf),
+                                         buf.numel(), _stream())
+    else:
+        gs = (ctypes.c_float * E)(*[float(x) for x in (global_scales or [1.0] * E)])
+        st = L.petit_moe_gemm_bf16_nvfp4(_ptr(A), _ptr(rep), gs, off, E, _ptr(C), n, k, _ptr(buf),
+                                         buf.numel(), _stream())
+    _check(st, "moe_gemm_" + fmt)
     return C
 
 

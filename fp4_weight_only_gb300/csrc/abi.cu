@@ -126,6 +126,50 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Checks expert offsets: 1 <= E <= kMaxGroups, off[0] == 0, non-decreasing,
+// total rows <= kMaxDim.
+petit_status_t check_offsets(const int64_t* off, int64_t num_experts) {
+  if (!off || num_experts < 1) return PETIT_ERR_INVALID_ARG;
+  if (num_experts > petit::kMaxGroups) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  if (off[0] != 0) return PETIT_ERR_INVALID_ARG;
+  for (int64_t e = 0; e < num_experts; ++e)
+    if (off[e + 1] < off[e]) return PETIT_ERR_INVALID_ARG;
+  if (off[num_experts] > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  return PETIT_OK;
+}
+
+petit_status_t moe_common(int fmt, const void* A, const uint8_t* rep, const float* gscales,
+                          const int64_t* off, int64_t num_experts, void* C, int64_t n, int64_t k,
+                          void* ws, size_t ws_bytes, petit_stream_t stream) {
+  if (petit_status_t st = check_offsets(off, num_experts)) return st;
+  if (off[num_experts] == 0) return PETIT_OK;   // no routed tokens: nothing to compute
+  if (!A || !rep || !C) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (!aligned16(A) || !aligned16(rep) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
+  float alphas[petit::kMaxGroups];
+  for (int64_t e = 0; e < num_experts; ++e) {
+    const float g = gscales ? gscales[e] : 1.0f;
+    if (!(g > 0.0f) || g > 1.0e36f) return PETIT_ERR_INVALID_ARG;
+    // NVFP4's register decode yields Wq * 2^-8; the epilogue restores it
+    alphas[e] = fmt == kNVFP4 ? g * 256.0f : 1.0f;
+  }
+  const int64_t rows = off[num_experts];
+  if (!ws) return PETIT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
+  int sms = 0;
+  if (petit_status_t st = current_device(&sms)) return st;
+  const petit::GemmPlan plan =
+      petit::plan_grouped(off, static_cast<int>(num_experts), n, k, fmt, sms);
+  if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (petit_status_t st = encode_a_map(&map, A, rows, k, plan.bn, plan.ku)) return st;
+  petit::GemmArgs args{A, rep, C, rows, n, k, alphas[0], static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  args.rep_stride = static_cast<int64_t>(petit_repacked_bytes(n, k, fmt));
+  args.group_alpha = alphas;
+  return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -160,6 +204,34 @@ size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt) {
   int sms = 0;
   if (current_device(&sms) != PETIT_OK) return 0;
   return petit::plan_gemm(m, n, k, fmt, sms).ws.total;
+}
+
+size_t petit_moe_workspace_bytes(const int64_t* expert_offsets, int64_t num_experts, int64_t n,
+                                 int64_t k, int fmt) {
+  if (check_offsets(expert_offsets, num_experts) != PETIT_OK || check_tiled_shape(n, k) != PETIT_OK)
+    return 0;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return 0;
+  int sms = 0;
+  if (current_device(&sms) != PETIT_OK) return 0;
+  return petit::plan_grouped(expert_offsets, static_cast<int>(num_experts), n, k, fmt, sms).ws.total;
+}
+
+petit_status_t petit_moe_gemm_bf16_mxfp4(const void* A, const uint8_t* rep,
+                                         const int64_t* expert_offsets, int64_t num_experts,
+                                         void* C, int64_t n, int64_t k, void* workspace,
+                                         size_t workspace_bytes, petit_stream_t stream) {
+  return moe_common(kMXFP4, A, rep, nullptr, expert_offsets, num_experts, C, n, k, workspace,
+                    workspace_bytes, stream);
+}
+
+petit_status_t petit_moe_gemm_bf16_nvfp4(const void* A, const uint8_t* rep,
+                                         const float* global_scales, const int64_t* expert_offsets,
+                                         int64_t num_experts, void* C, int64_t n, int64_t k,
+                                         void* workspace, size_t workspace_bytes,
+                                         petit_stream_t stream) {
+  if (!global_scales) return PETIT_ERR_INVALID_ARG;
+  return moe_common(kNVFP4, A, rep, global_scales, expert_offsets, num_experts, C, n, k, workspace,
+                    workspace_bytes, stream);
 }
 
 petit_status_t petit_absmax_bf16(const void* x, int64_t count, float* amax_out,

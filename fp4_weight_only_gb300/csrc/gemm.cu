@@ -53,19 +53,64 @@ constexpr uint32_t kTmemCols = 512;
 
 struct Params {
   const uint8_t* rep;
-  uint16_t* c;              // BF16 (or FP16 for the FP16 layout) [m][n]
+  uint16_t* c;              // BF16 (or FP16 for the FP16 layout) [rows][n]
   float* partials;
   uint32_t* counters;
   uint32_t* status;
-  int32_t m, n;
-  int32_t m_tiles, k_units;   // units per tile row = k / (128 * KU)
+  int32_t n, n_tiles;
+  int32_t k_units;          // units per tile = k / (128 * KU)
   int64_t units;
   int32_t num_ctas;
-  float alpha;
+  int32_t weights_reused;   // a group has several activation tiles
   uint64_t timeout_ns;
   const float* alpha_dev;   // nullable: device-resident factor, times alpha_scale
   float alpha_scale;
+  int64_t rep_stride;       // bytes between groups' repacked weights
+  int32_t num_groups;
+  int32_t row_off[kMaxGroups + 1];    // group g: activation / output rows
+  int32_t tile_base[kMaxGroups + 1];  // group g: first tile
+  float group_alpha[kMaxGroups];      // epilogue factor per group
 };
+
+// Position of a tile: group, weight tile, activation tile (tile-major in a
+// group, groups in order).  Walked tile by tile without divisions.
+struct TileCursor {
+  int32_t g;
+  int32_t m_tiles;   // activation tiles of group g
+  int32_t nt, mt;
+  int32_t row0;      // first activation row of group g
+};
+
+template <int BN>
+__device__ __forceinline__ int32_t group_m_tiles(const Params& p, int g) {
+  return (p.row_off[g + 1] - p.row_off[g] + BN - 1) / BN;
+}
+
+template <int BN>
+__device__ __forceinline__ TileCursor cursor_at(const Params& p, int64_t tile) {
+  TileCursor c;
+  c.g = 0;
+  while (c.g + 1 < p.num_groups && p.tile_base[c.g + 1] <= tile) ++c.g;
+  c.m_tiles = group_m_tiles<BN>(p, c.g);
+  c.row0 = p.row_off[c.g];
+  const int32_t local = static_cast<int32_t>(tile - p.tile_base[c.g]);
+  c.nt = c.m_tiles > 0 ? local / c.m_tiles : 0;
+  c.mt = c.m_tiles > 0 ? local - c.nt * c.m_tiles : 0;
+  return c;
+}
+
+template <int BN>
+__device__ __forceinline__ void cursor_next(const Params& p, TileCursor& c) {
+  if (++c.mt < c.m_tiles) return;
+  c.mt = 0;
+  if (++c.nt < p.n_tiles) return;
+  c.nt = 0;
+  do {
+    ++c.g;
+  } while (c.g < p.num_groups && group_m_tiles<BN>(p, c.g) == 0);
+  c.m_tiles = c.g < p.num_groups ? group_m_tiles<BN>(p, c.g) : 0;
+  c.row0 = c.g < p.num_groups ? p.row_off[c.g] : 0;
+}
 
 template <int FMT, int BN, int KU>
 struct Cfg {
@@ -216,15 +261,14 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     // (while the previous kernel finishes); the copies after the wait then
     // hit L2.
     const int64_t tile0 = u0 / KS;
-    int64_t ku = u0 - tile0 * KS, nt = tile0 / p.m_tiles, mt = tile0 - nt * p.m_tiles;
+    int64_t ku = u0 - tile0 * KS;
+    TileCursor cur = cursor_at<BN>(p, tile0);
     for (int64_t u = u0; u < u1 && u < u0 + C::kWStages; ++u) {
-      bulk_prefetch_l2(p.rep + chunk_offset<FMT>(nt, ku * KU, KS * KU), C::kWBytes);
+      bulk_prefetch_l2(p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, ku * KU, KS * KU),
+                       C::kWBytes);
       if (++ku == KS) {
         ku = 0;
-        if (++mt == p.m_tiles) {
-          mt = 0;
-          ++nt;
-        }
+        cursor_next<BN>(p, cur);
       }
     }
   }
@@ -253,7 +297,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     if (lane == 0) {
       // weights are streamed once (evict first) unless several m-tiles
       // revisit them, in which case the revisits should hit L2
-      const uint64_t policy = p.m_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t policy = p.weights_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
       // Two streams over the same units: weight chunks (stage freed by the
       // dequantisers) and activation tiles (freed by the MMAs).  Whichever
       // has a free stage is issued next, weights first.  All per-unit
@@ -265,8 +309,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       int64_t wi = 0, xi = 0;           // next unit (CTA-local) of each stream
       int ws = 0, xs = 0;               // their stages and phases
       uint32_t wph = 0, xph = 0;
-      int64_t w_ku = ku0, w_nt = tile0 / p.m_tiles, w_mt = tile0 - w_nt * p.m_tiles;
-      int64_t x_ku = ku0, x_mt = w_mt;
+      int64_t w_ku = ku0, x_ku = ku0;
+      TileCursor wc = cursor_at<BN>(p, tile0), xc = wc;
       const uint64_t t0 = global_timer_ns();
       for (uint32_t spin = 0; wi < nu || xi < nu;) {
         bool progress = false;
@@ -274,7 +318,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           const uint32_t fb = smem_u32(&wfull[ws]);
           mbar_arrive_expect_tx(fb, C::kWBytes);
           bulk_g2s(smem_u32(sm_w + ws * C::kWBytes),
-                   p.rep + chunk_offset<FMT>(w_nt, w_ku * KU, KS * KU), C::kWBytes, fb, policy);
+                   p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, w_ku * KU, KS * KU),
+                   C::kWBytes, fb, policy);
           ++wi;
           if (++ws == C::kWStages) {
             ws = 0;
@@ -282,17 +327,15 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           }
           if (++w_ku == KS) {
             w_ku = 0;
-            if (++w_mt == p.m_tiles) {
-              w_mt = 0;
-              ++w_nt;
-            }
+            cursor_next<BN>(p, wc);
           }
           progress = true;
         }
         if (xi < nu && mbar_test_wait(smem_u32(&mdone[xs]), xph ^ 1u)) {
           const uint32_t fb = smem_u32(&xfull[xs]);
           mbar_arrive_expect_tx(fb, C::kABytes);
-          tma_load_3d(smem_u32(sm_a + xs * C::kABytes), &tmap_a, 0, static_cast<int32_t>(x_mt * BN),
+          tma_load_3d(smem_u32(sm_a + xs * C::kABytes), &tmap_a, 0,
+                      static_cast<int32_t>(xc.row0 + xc.mt * BN),
                       static_cast<int32_t>(x_ku * 2 * KU), fb);
           ++xi;
           if (++xs == C::kXStages) {
@@ -301,7 +344,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           }
           if (++x_ku == KS) {
             x_ku = 0;
-            if (++x_mt == p.m_tiles) x_mt = 0;
+            cursor_next<BN>(p, xc);
           }
           progress = true;
         }
@@ -393,7 +436,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     const int64_t first_tile_of_cta = u0 / KS;
     // epilogue factor: a device-resident global scale is read here, after the
     // grid dependency wait, so a preceding kernel may have produced it
-    const float alpha = p.alpha_dev ? p.alpha_scale * *p.alpha_dev : p.alpha;
+    const float alpha_dev = p.alpha_dev ? p.alpha_scale * *p.alpha_dev : 0.0f;
+    TileCursor ec = cursor_at<BN>(p, first_tile_of_cta);   // advances one tile per segment
     uint32_t epi_phase = 0;
     // bounded barrier among the four epilogue warps (a hardware named
     // barrier has no time limit)
@@ -408,7 +452,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const int64_t tile = u / KS;
       const int64_t seg_end = (tile + 1) * KS < u1 ? (tile + 1) * KS : u1;
       const bool full_tile = (u == tile * KS) && (seg_end == (tile + 1) * KS);
-      const int64_t nt = tile / p.m_tiles, mt = tile % p.m_tiles;
+      const int64_t nt = ec.nt, mt = ec.mt;
+      const int64_t g_rows = p.row_off[ec.g + 1] - p.row_off[ec.g];  // this group's activation rows
+      uint16_t* const c_g = p.c + static_cast<int64_t>(p.row_off[ec.g]) * p.n;
+      const float alpha = p.alpha_dev ? alpha_dev : p.group_alpha[ec.g];
+      cursor_next<BN>(p, ec);
       const int d = static_cast<int>(seg % C::kNumD);
       if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
@@ -446,8 +494,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-            if (mrow < p.m)
-              p.c[mrow * p.n + ncol] = out_bits<FMT>(alpha * __uint_as_float(v[j]));
+            if (mrow < g_rows) c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * __uint_as_float(v[j]));
           }
         } else {
 #pragma unroll
@@ -511,7 +558,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-              if (mrow < p.m) p.c[mrow * p.n + ncol] = out_bits<FMT>(alpha * acc[j]);
+              if (mrow < g_rows) c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * acc[j]);
             }
           }
         }
@@ -650,23 +697,54 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
+GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
+                      int num_sms) {
   GemmPlan pl{};
   pl.fmt = fmt;
+  pl.num_groups = num_groups;
+  int64_t max_rows = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    const int64_t r = row_off[g + 1] - row_off[g];
+    if (r > max_rows) max_rows = r;
+  }
+  const int64_t m = max_rows > 0 ? max_rows : 1;
   pl.bn = m <= 16 ? 16 : (m <= 32 ? 32 : (m <= 64 ? 64 : (m <= 128 ? 128 : 256)));
-  if (pl.bn == 256 && m <= 256) {
+  if (num_groups > 1) {
+    // groups of different sizes share one tile height: take the one with the
+    // least work, counting each activation tile as one pass over the group's
+    // weights and an N = 256 tile as two (its MMAs, not the weight stream,
+    // set its pace)
+    int64_t best = -1;
+    for (int bn = 16; bn <= 256; bn *= 2) {
+      int64_t tiles = 0;
+      for (int g = 0; g < num_groups; ++g) tiles += (row_off[g + 1] - row_off[g] + bn - 1) / bn;
+      const int64_t cost = tiles * (bn > 128 ? bn / 128 : 1);
+      if (best < 0 || cost < best) {
+        best = cost;
+        pl.bn = bn;
+      }
+    }
+  } else if (pl.bn == 256 && m <= 256) {
     // N = 256 dequantises each weight once for all rows, but halves the
     // number of work units; small matrices keep two 128-row tiles so that
     // every CTA still has a long pipeline to amortise its fixed costs over
-    const int64_t units256 = (n / kTileN) * (k / kStageK);
+    const int64_t units256 = num_groups * (n / kTileN) * (k / kStageK);
     if (units256 < 48 * static_cast<int64_t>(num_sms)) pl.bn = 128;
   }
   // two chunks per unit halves the copy requests when the A tile is small
   pl.ku = (pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
-  pl.m_tiles = static_cast<int>((m + pl.bn - 1) / pl.bn);
   pl.n_tiles = static_cast<int>(n / kTileN);
   pl.k_stages = static_cast<int>(k / kStageK);
-  pl.units = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles * (pl.k_stages / pl.ku);
+  int64_t tiles = 0;
+  for (int g = 0; g <= num_groups; ++g) {
+    pl.row_off[g] = static_cast<int32_t>(row_off[g]);
+    pl.tile_base[g] = static_cast<int32_t>(tiles);
+    if (g == num_groups) break;
+    const int64_t mt = (row_off[g + 1] - row_off[g] + pl.bn - 1) / pl.bn;
+    if (mt > 1) pl.weights_reused = true;
+    tiles += mt * pl.n_tiles;
+  }
+  pl.units = tiles * (pl.k_stages / pl.ku);
   pl.num_ctas = static_cast<int>(pl.units < num_sms ? pl.units : num_sms);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
   if (pl.num_ctas > kMaxCtas) pl.num_ctas = kMaxCtas;
@@ -677,6 +755,11 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
   return pl;
 }
 
+GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
+  const int64_t off[2] = {0, m};
+  return plan_grouped(off, 1, n, k, fmt, num_sms);
+}
+
 cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap& tmap,
                         cudaStream_t stream) {
   Params prm{};
@@ -685,16 +768,23 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   prm.partials = reinterpret_cast<float*>(a.workspace + pl.ws.partials_off);
   prm.counters = reinterpret_cast<uint32_t*>(a.workspace + pl.ws.counters_off);
   prm.status = reinterpret_cast<uint32_t*>(a.workspace);
-  prm.m = static_cast<int32_t>(a.m);
   prm.n = static_cast<int32_t>(a.n);
-  prm.m_tiles = pl.m_tiles;
+  prm.n_tiles = pl.n_tiles;
   prm.k_units = pl.k_stages / pl.ku;
   prm.units = pl.units;
   prm.num_ctas = pl.num_ctas;
-  prm.alpha = a.alpha;
+  prm.weights_reused = pl.weights_reused ? 1 : 0;
   prm.alpha_dev = a.alpha_dev;
   prm.alpha_scale = a.alpha_scale;
   prm.timeout_ns = a.timeout_ns;
+  prm.rep_stride = a.rep_stride;
+  prm.num_groups = pl.num_groups;
+  for (int g = 0; g <= pl.num_groups; ++g) {
+    prm.row_off[g] = pl.row_off[g];
+    prm.tile_base[g] = pl.tile_base[g];
+  }
+  for (int g = 0; g < pl.num_groups; ++g)
+    prm.group_alpha[g] = a.group_alpha ? a.group_alpha[g] : a.alpha;
   if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream);
   if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream);
   return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream);

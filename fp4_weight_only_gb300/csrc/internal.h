@@ -27,19 +27,31 @@ struct WsLayout {
   size_t total;
 };
 
+// A launch computes one GEMM or a group of GEMMs that share n and k (the
+// experts of an MoE layer): group g multiplies activation rows
+// [row_off[g], row_off[g+1]) by its own weights.  Tiles are numbered group by
+// group (tile_base[g] is group g's first), weight-tile-major within a group.
+constexpr int kMaxGroups = 64;
+
 struct GemmPlan {
   int fmt;
   int bn;          // activation rows per tile (MMA N)
   int ku;          // 128-k chunks per pipeline unit (1 or 2)
-  int m_tiles;
   int n_tiles;
   int k_stages;    // 128-k chunks per tile row
-  int64_t units;   // n_tiles * m_tiles * k_stages / ku
+  int64_t units;   // tiles * k_stages / ku
   int num_ctas;
+  bool weights_reused;   // some group has several activation tiles
+  int num_groups;
+  int32_t row_off[kMaxGroups + 1];
+  int32_t tile_base[kMaxGroups + 1];
   WsLayout ws;
 };
 
 GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
+// row_off: num_groups + 1 non-decreasing offsets starting at 0
+GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
+                      int num_sms);
 
 struct GemmArgs {
   const void* A;
@@ -53,6 +65,10 @@ struct GemmArgs {
   // device after the preceding kernel on the stream has completed
   const float* alpha_dev = nullptr;
   float alpha_scale = 1.0f;
+  // groups: bytes between consecutive groups' repacked weights, and each
+  // group's epilogue factor (host array of num_groups; null: alpha for all)
+  int64_t rep_stride = 0;
+  const float* group_alpha = nullptr;
 };
 
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, const CUtensorMap& tmap_a,

@@ -54,3 +54,23 @@ def one_hot_activations(m, k, cols, device="cpu"):
     idx = torch.as_tensor(cols, dtype=torch.long, device=device)
     a[torch.arange(m, device=device), idx] = 1.0
     return a
+
+
+def moe_expert_offsets(tokens, experts, top_k, seed=0, skew=1.0):
+    """Synthetic MoE routing: each of `tokens` tokens picks `top_k` distinct
+    experts with probability proportional to 1 / (rank + 1)^skew (a seeded,
+    Zipf-like popularity over a seeded expert order).  Returns the E + 1
+    row offsets of the expert-grouped activation matrix (tokens * top_k
+    rows)."""
+    g = _gen(seed, "cpu")
+    order = torch.randperm(experts, generator=g)
+    weights = torch.empty(experts)
+    weights[order] = 1.0 / (torch.arange(experts, dtype=torch.float32) + 1.0) ** skew
+    counts = torch.zeros(experts, dtype=torch.int64)
+    for _ in range(tokens):
+        picked = torch.multinomial(weights, top_k, replacement=False, generator=g)
+        counts[picked] += 1
+    offsets = [0]
+    for c in counts.tolist():
+        offsets.append(offsets[-1] + c)
+    return offsets

@@ -213,6 +213,36 @@ petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,
                                      void* workspace, size_t workspace_bytes,
                                      petit_stream_t stream);
 
+/* --------------------------------------------------- MoE grouped GEMM */
+
+/* Mixture-of-experts layer GEMM (Petit PyPI page, "Features": fused MoE
+ * kernels for BF16 x MXFP4): num_experts GEMMs that share n and k in one
+ * launch, stream-K balanced over all of them.  Expert e multiplies the
+ * activation rows [off[e], off[e+1]) of A (BF16 [T][k], T = off[E]; the
+ * caller groups the routed tokens by expert) by its own weights and writes
+ * the same rows of C (BF16 [T][n]):
+ *   C[r][:] = g_e * A[r][:] . Wq_e^T,   off[e] <= r < off[e+1].
+ * rep holds the experts' repacked weights back to back, each
+ * petit_repacked_bytes(n, k, fmt) bytes (petit_repack_mxfp4 / _nvfp4 output).
+ * expert_offsets: host array of num_experts + 1 values, off[0] = 0,
+ * non-decreasing (empty experts allowed); 1 <= num_experts <= 64.
+ * global_scales (NVFP4 only): host array of num_experts positive floats.
+ * workspace: at least petit_moe_workspace_bytes(...) bytes, as for
+ * petit_gemm_bf16_nvfp4.  T = 0 is a no-op.  Errors: INVALID_ARG (offsets
+ * or scales), UNSUPPORTED_SHAPE (more than 64 experts, n or k not multiples
+ * of 128), MISALIGNED, WORKSPACE, ARCH, CUDA. */
+size_t petit_moe_workspace_bytes(const int64_t* expert_offsets, int64_t num_experts, int64_t n,
+                                 int64_t k, int fmt);
+petit_status_t petit_moe_gemm_bf16_mxfp4(const void* A, const uint8_t* rep,
+                                         const int64_t* expert_offsets, int64_t num_experts,
+                                         void* C, int64_t n, int64_t k, void* workspace,
+                                         size_t workspace_bytes, petit_stream_t stream);
+petit_status_t petit_moe_gemm_bf16_nvfp4(const void* A, const uint8_t* rep,
+                                         const float* global_scales, const int64_t* expert_offsets,
+                                         int64_t num_experts, void* C, int64_t n, int64_t k,
+                                         void* workspace, size_t workspace_bytes,
+                                         petit_stream_t stream);
+
 /* NVFP4 GEMM without a workspace argument.  The pages have no counterpart to
  * this entry point; it is for callers that cannot allocate device memory at
  * the time they call the GEMM: code running while a CUDA graph is being
