@@ -50,6 +50,7 @@ constexpr int kDeqWarp0 = 6;    // dequantiser warps 6 .. 6 + 4 * groups - 1
 constexpr int kDeqGroupWarps = 4;   // one dequantiser group: a warp per lane quarter
 constexpr int kMaxMmaThreads = 3;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kFixBatch = 2;   // split-tile contributors whose partials are loaded together
 
 struct Params {
   const uint8_t* rep;
@@ -511,12 +512,14 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         // every contributor but the first starts inside this tile (slot 2c);
         // the first uses its second slot unless its range starts at the tile
         const int64_t first_slot = 2 * c_first + ((c_first * U / P) / KS == tile ? 0 : 1);
-        __threadfence();
+        // Ordering without per-thread fences: the group barrier (mbarrier
+        // arrive = release, wait = acquire, CTA scope) orders every epilogue
+        // thread's partial stores before thread 0's GPU-scope acq_rel
+        // arrival, which releases them cumulatively to the CTA that acquires
+        // the counter last; that CTA's acquire reaches its other epilogue
+        // threads through its own group barrier before their loads.
         if (!epi_sync()) break;
         if (epi_tid == 0) {
-          // acq_rel at GPU scope: releases the partials this CTA's epilogue
-          // threads stored (ordered before this point by their fences and
-          // the group barrier) and acquires those of earlier arrivals
           const uint32_t old = atomic_add_acq_rel_gpu(&p.counters[c_first], 1u);
           const int is_last = (static_cast<int64_t>(old) == c_last - c_first);
           if (is_last) atomicExch(&p.counters[c_first], 0u);  // ready for the next call
@@ -524,9 +527,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         }
         if (!epi_sync()) break;
         if (*epi_flag) {
-          __threadfence();
           // contributors' partials are summed in CTA order (deterministic);
-          // loads are batched (up to 2 contributors x 16 columns in flight)
+          // loads are batched (kFixBatch contributors x 16 columns in flight),
           // so the reduction costs a few L2 round trips, not one per value
 #pragma unroll 1
           for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -534,10 +536,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll 1
-            for (int64_t cb = c_first; cb <= c_last; cb += 2) {
-              float t[2][16];
+            for (int64_t cb = c_first; cb <= c_last; cb += kFixBatch) {
+              float t[kFixBatch][16];
 #pragma unroll
-              for (int x = 0; x < 2; ++x) {
+              for (int x = 0; x < kFixBatch; ++x) {
                 const int64_t c = cb + x;
                 if (c <= c_last) {
                   const int64_t cs = c == c_first ? first_slot : 2 * c;
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
                 }
               }
 #pragma unroll
-              for (int x = 0; x < 2; ++x) {
+              for (int x = 0; x < kFixBatch; ++x) {
                 if (cb + x <= c_last) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
