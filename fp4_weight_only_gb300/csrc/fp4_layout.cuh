@@ -20,7 +20,7 @@
 
 namespace petit {
 
-constexpr int kLayoutVersion = 2;
+constexpr int kLayoutVersion = 3;
 constexpr int kTileN = 128;   // weight rows per tile (the MMA M side)
 constexpr int kStageK = 128;  // k elements per repacked chunk / pipeline stage
 constexpr int kWChunkBytes = kTileN * kStageK / 2;  // 8192
@@ -67,24 +67,21 @@ __host__ __device__ constexpr size_t chunk_offset(int64_t tile, int64_t stage, i
   return static_cast<size_t>((tile * stages + stage) * FmtTraits<FMT>::kChunkBytes);
 }
 
-// Bit position of each code's bits (sign, e1, e0, m) in a 32-bit word:
-//   c0: 15  8  7  6     c1: 31 24 23 22     (decode: q & M)
-//   c2: 12  5  4  3     c3: 28 21 20 19     (decode: (q << 3) & M)
-//   c4:  9  2  1  0     c5: 25 18 17 16     (decode: (q << 6) & M)
-//   c6: 11 14 13 10     c7: 27 30 29 26     (decode: three shifts)
-// with M = 0x81C081C0 selecting BF16 bits {15, 8, 7, 6} of both halves.
+// Bit positions of each code's bits (m, e0, e1, s) in a 32-bit word:
+//   c0:  6  7  8 15     c1: 22 23 24 31     (decode: q & M)
+//   c2:  0  1  2  9     c3: 16 17 18 25     (decode: (q << 6) & M)
+//   c4: 26 27 28  3     c5: 10 11 12 19     (decode: rotl(q, 12) & M)
+//   c6:  4  5 30 13     c7: 20 21 14 29     (decode: (q << 2) & M' | rotl(q, 10) & M'')
+// with M = 0x81C081C0 selecting BF16 bits {15, 8, 7, 6} of both halves,
+// M' = 0x80C080C0 and M'' = 0x01000100.  Nine integer operations per word, two
+// of them rotates (funnel shifts): an exhaustive search shows that no four
+// rotated copies of M tile the word, so one output merges two rotations.
 __host__ __device__ inline uint32_t pack_word(const uint32_t (&c)[8]) {
-  auto mag = [](uint32_t x) { return x & 7u; };
-  auto sgn = [](uint32_t x) { return (x >> 3) & 1u; };
+  constexpr int pos[8][4] = {{6, 7, 8, 15},   {22, 23, 24, 31}, {0, 1, 2, 9},     {16, 17, 18, 25},
+                             {26, 27, 28, 3}, {10, 11, 12, 19}, {4, 5, 30, 13},   {20, 21, 14, 29}};
   uint32_t q = 0;
-  q |= (mag(c[0]) << 6) | (sgn(c[0]) << 15);
-  q |= (mag(c[1]) << 22) | (sgn(c[1]) << 31);
-  q |= (mag(c[2]) << 3) | (sgn(c[2]) << 12);
-  q |= (mag(c[3]) << 19) | (sgn(c[3]) << 28);
-  q |= (mag(c[4]) << 0) | (sgn(c[4]) << 9);
-  q |= (mag(c[5]) << 16) | (sgn(c[5]) << 25);
-  q |= (((c[6] >> 1) & 3u) << 13) | ((c[6] & 1u) << 10) | (sgn(c[6]) << 11);
-  q |= (((c[7] >> 1) & 3u) << 29) | ((c[7] & 1u) << 26) | (sgn(c[7]) << 27);
+  for (int i = 0; i < 8; ++i)
+    for (int b = 0; b < 4; ++b) q |= ((c[i] >> b) & 1u) << pos[i][b];
   return q;
 }
 
@@ -113,9 +110,9 @@ __host__ __device__ inline uint32_t pack_word_f16(const uint32_t (&c)[8]) {
 __device__ __forceinline__ void decode_word_raw(uint32_t q, uint32_t (&p)[4]) {
   constexpr uint32_t M = 0x81C081C0u;
   p[0] = q & M;
-  p[1] = (q << 3) & M;
-  p[2] = (q << 6) & M;
-  p[3] = ((q >> 6) & 0x01800180u) | ((q >> 4) & 0x00400040u) | ((q << 4) & 0x80008000u);
+  p[1] = (q << 6) & M;
+  p[2] = __funnelshift_l(q, q, 12) & M;
+  p[3] = ((q << 2) & 0x80C080C0u) | (__funnelshift_l(q, q, 10) & 0x01000100u);
 }
 
 // Four FP16x2 words value(c_i) * 2^-14 for the pairs (c0,c1) .. (c6,c7) of a
