@@ -308,44 +308,59 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const int64_t tile0 = u0 / KS;
       const int64_t ku0 = u0 - tile0 * KS;
       int64_t wi = 0, xi = 0;           // next unit (CTA-local) of each stream
-      int ws = 0, xs = 0;               // their stages and phases
       uint32_t wph = 0, xph = 0;
-      int64_t w_ku = ku0, x_ku = ku0;
+      int32_t w_ku = static_cast<int32_t>(ku0), x_ku = w_ku;
       TileCursor wc = cursor_at<BN>(p, tile0), xc = wc;
+      // running addresses: the consecutive units of a tile are adjacent
+      // chunks, so the weight source advances by one unit's bytes and is
+      // recomputed only at a tile boundary; stage addresses advance by one
+      // stage and wrap
+      const uint8_t* wsrc =
+          p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, w_ku * KU, KS * KU);
+      int32_t xrow = xc.row0 + xc.mt * BN, xk = x_ku * 2 * KU;
+      const uint32_t wdst0 = smem_u32(sm_w), xdst0 = smem_u32(sm_a);
+      const uint32_t wfree0 = smem_u32(&wfree[0]), wfull0 = smem_u32(&wfull[0]);
+      const uint32_t mdone0 = smem_u32(&mdone[0]), xfull0 = smem_u32(&xfull[0]);
+      uint32_t wdst = wdst0, xdst = xdst0, wbar = 0, xbar = 0;   // bar: stage * 8
       const uint64_t t0 = global_timer_ns();
       for (uint32_t spin = 0; wi < nu || xi < nu;) {
         bool progress = false;
-        if (wi < nu && mbar_test_wait(smem_u32(&wfree[ws]), wph ^ 1u)) {
-          const uint32_t fb = smem_u32(&wfull[ws]);
-          mbar_arrive_expect_tx(fb, C::kWBytes);
-          bulk_g2s(smem_u32(sm_w + ws * C::kWBytes),
-                   p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, w_ku * KU, KS * KU),
-                   C::kWBytes, fb, policy);
+        if (wi < nu && mbar_test_wait(wfree0 + wbar, wph ^ 1u)) {
+          mbar_arrive_expect_tx(wfull0 + wbar, C::kWBytes);
+          bulk_g2s(wdst, wsrc, C::kWBytes, wfull0 + wbar, policy);
           ++wi;
-          if (++ws == C::kWStages) {
-            ws = 0;
+          wsrc += C::kWBytes;
+          wdst += C::kWBytes;
+          wbar += 8;
+          if (wbar == 8 * C::kWStages) {
+            wbar = 0;
+            wdst = wdst0;
             wph ^= 1u;
           }
           if (++w_ku == KS) {
             w_ku = 0;
             cursor_next<BN>(p, wc);
+            wsrc = p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, 0, KS * KU);
           }
           progress = true;
         }
-        if (xi < nu && mbar_test_wait(smem_u32(&mdone[xs]), xph ^ 1u)) {
-          const uint32_t fb = smem_u32(&xfull[xs]);
-          mbar_arrive_expect_tx(fb, C::kABytes);
-          tma_load_3d(smem_u32(sm_a + xs * C::kABytes), &tmap_a, 0,
-                      static_cast<int32_t>(xc.row0 + xc.mt * BN),
-                      static_cast<int32_t>(x_ku * 2 * KU), fb);
+        if (xi < nu && mbar_test_wait(mdone0 + xbar, xph ^ 1u)) {
+          mbar_arrive_expect_tx(xfull0 + xbar, C::kABytes);
+          tma_load_3d(xdst, &tmap_a, 0, xrow, xk, xfull0 + xbar);
           ++xi;
-          if (++xs == C::kXStages) {
-            xs = 0;
+          xk += 2 * KU;
+          xdst += C::kABytes;
+          xbar += 8;
+          if (xbar == 8 * C::kXStages) {
+            xbar = 0;
+            xdst = xdst0;
             xph ^= 1u;
           }
           if (++x_ku == KS) {
             x_ku = 0;
+            xk = 0;
             cursor_next<BN>(p, xc);
+            xrow = xc.row0 + xc.mt * BN;
           }
           progress = true;
         }
