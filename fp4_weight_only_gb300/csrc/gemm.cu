@@ -73,6 +73,19 @@ struct Params {
   float group_alpha[kMaxGroups];      // epilogue factor per group
 };
 
+// The split-tile fix-up of a CTA's last segment, when this CTA arrives last
+// on that tile.  It is deferred to after the kernel's final barrier so that
+// every warp shares it: with BN = 256 the tile's partials are 128 KB per
+// contributor, which the four epilogue warps alone would sum in sixteen
+// dependent 16-column rounds at the end of the kernel.
+struct FixJob {
+  uint16_t* c_g;                        // output rows of the tile's group
+  int64_t c_first, c_last, first_slot;  // contributing CTAs, slot of the first
+  int64_t row0, col0, g_rows;           // tile origin in C; rows of the group
+  float alpha;
+  int32_t valid;
+};
+
 // Position of a tile: group, weight tile, activation tile (tile-major in a
 // group, groups in order).  Walked tile by tile without divisions.
 struct TileCursor {
@@ -175,6 +188,11 @@ struct Cfg {
                     kNumA % kMmaThreads == 0 && kNumA <= kXStages,
                 "fixed consumer per barrier");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  // barriers, tensor-memory holder, flags and the deferred fix-up job fit in
+  // the 1024 bytes after the rings
+  static_assert((2 * kWStages + 2 * kXStages + kNumA + 2 * kNumD + kMaxMmaThreads + 1) * 8 + 16 +
+                        sizeof(FixJob) + 16 <= 1024,
+                "barrier region");
 };
 
 // Output element bits: BF16, or FP16 for the FP16-activation layout (RNE).
@@ -220,6 +238,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_flag = abort_flag + 1;
+  FixJob* fix = reinterpret_cast<FixJob*>(
+      (reinterpret_cast<uintptr_t>(epi_flag + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -248,6 +268,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     mbar_init(smem_u32(epi_bar), 4);
     *abort_flag = 0;
     *epi_flag = 0;
+    fix->valid = 0;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -541,7 +562,20 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           *epi_flag = is_last;
         }
         if (!epi_sync()) break;
-        if (*epi_flag) {
+        if (*epi_flag && seg_end == u1) {
+          // the CTA's last segment: summed by all warps after the final barrier
+          if (epi_tid == 0) {
+            fix->c_g = c_g;
+            fix->c_first = c_first;
+            fix->c_last = c_last;
+            fix->first_slot = first_slot;
+            fix->row0 = static_cast<int64_t>(mt) * BN;
+            fix->col0 = static_cast<int64_t>(nt) * kTileN;
+            fix->g_rows = g_rows;
+            fix->alpha = alpha;
+            fix->valid = 1;
+          }
+        } else if (*epi_flag) {
           // contributors' partials are summed in CTA order (deterministic);
           // loads are batched (kFixBatch contributors x 16 columns in flight),
           // so the reduction costs a few L2 round trips, not one per value
@@ -662,6 +696,54 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+
+  // Deferred fix-up of the last segment's tile (see FixJob), by all threads:
+  // element e = activation row * 128 + weight row, as in a partial slot, so
+  // consecutive threads read and write consecutive addresses.  Partials are
+  // added in CTA order, as in the epilogue.  The epilogue's acquire of the
+  // arrival counter reaches every thread through the barrier above.
+  if (fix->valid && !*abort_flag) {
+    const FixJob f = *fix;
+    constexpr int kElems = BN * kTileN;
+    constexpr int kStride = C::kThreads;
+#pragma unroll 1
+    for (int e0 = threadIdx.x; e0 < kElems; e0 += 16 * kStride) {
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+      for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
+        float t[kFixBatch][16];
+#pragma unroll
+        for (int x = 0; x < kFixBatch; ++x) {
+          const int64_t c = cb + x;
+          if (c <= f.c_last) {
+            const float* src =
+                p.partials + static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * c) * kElems;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int e = e0 + j * kStride;
+              t[x][j] = e < kElems ? __ldcg(src + e) : 0.0f;
+            }
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < kFixBatch; ++x) {
+          if (cb + x <= f.c_last) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int e = e0 + j * kStride;
+        const int64_t mrow = f.row0 + (e >> 7);
+        if (e < kElems && mrow < f.g_rows)
+          f.c_g[mrow * p.n + f.col0 + (e & (kTileN - 1))] = out_bits<FMT>(f.alpha * acc[j]);
+      }
+    }
+  }
 }
 
 template <int FMT, int BN, int KU>
