@@ -7,6 +7,7 @@ there is no CPU fallback.
 """
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -81,6 +82,8 @@ class PetitError(RuntimeError):
 def load(build=True):
     """Build (if stale) and load the CUDA library; raises on failure."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.build() if build else _build.LIB
@@ -102,12 +105,19 @@ def _check(status, where):
         raise PetitError(status, where)
 
 
+# The raw handle of torch's current stream without building a Stream object
+# (a per-call cost on the GEMM path); the public call where it is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _need(t, dtype, name):
@@ -175,6 +185,7 @@ def dequant(rep, n, k, fmt="nvfp4"):
     return out
 
 
+@functools.lru_cache(maxsize=1024)
 def workspace_bytes(m, n, k, fmt="nvfp4"):
     return int(load().petit_gemm_workspace_bytes(m, n, k, FORMATS[fmt]))
 
