@@ -182,6 +182,13 @@ def synth_inputs_cpu(rows):
     return ws, acts
 
 
+def decode_config(world):
+    """The workload both arms report (the reference arm times a sample of it)."""
+    return {"workload": "llama3-70b linears qkv/o/gate_up/down, NVFP4 decode m=16, g=1",
+            "m": M_DECODE, "shapes_nk": [[n, k] for _, n, k in SHAPES],
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -202,8 +209,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "llama3-70b linears, NVFP4 decode m=16 (sample)",
-                                        "m": M_DECODE, "rows_per_matrix": rows},
+        "data": "synthetic", "config": decode_config(world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -529,10 +535,8 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights quantised to NVFP4 on the GPU)",
-            "config": {"workload": "llama3-70b linears qkv/o/gate_up/down, NVFP4 decode m=16, g=1",
-                       "m": M_DECODE, "shapes_nk": [[n, k] for _, n, k in SHAPES],
-                       "l2": "2 rotating weight sets of 481 MB each (> 129 MB L2)",
-                       "parallelism": f"replicas x{world}"},
+            "config": dict(decode_config(world),
+                           l2="2 rotating weight sets of 481 MB each (> 129 MB L2)"),
             "tflops": round(world * step_flops * args.steps / (elapsed_max * 1e-3) / 1e12, 2),
             "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
