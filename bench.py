@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--profile-only", action="store_true",
                    help="prepare one weight set and launch each decode GEMM once (for ncu captures)")
     p.add_argument("--profile-m", type=int, default=M_DECODE)
+    p.add_argument("--profile-fmt", choices=["nvfp4", "mxfp4", "nvfp4_f16"], default="nvfp4",
+                   help="weight format / activation type of the --profile-only launches")
     return p.parse_args()
 
 
@@ -556,17 +558,19 @@ def run_profile_only(args, local):
     torch.cuda.set_device(dev)
     binding.load()
     ws = binding.Workspace(dev)
-    m = args.profile_m
+    m, fmt = args.profile_m, args.profile_fmt
     for i, (name, n, k) in enumerate(SHAPES):
         w = synth.weights(n, k, seed=100 + i, device=dev)
-        fw = binding.FP4Weight(w, "nvfp4", 1.0)
+        fw = binding.FP4Weight(w, fmt, 1.0)
         del w
         a = synth.activations(m, k, seed=200 + i, device=dev)
+        if fmt == "nvfp4_f16":
+            a = a.to(torch.float16)
         fw(a, workspace=ws)
         torch.cuda.synchronize()
         del fw
     assert ws.status() == 0
-    print(f"profile-only: m={m} launched {len(SHAPES)} GEMMs", flush=True)
+    print(f"profile-only: {fmt} m={m} launched {len(SHAPES)} GEMMs", flush=True)
 
 
 def main():
