@@ -63,6 +63,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, device):
+    """The largest of x over all ranks of the process group (x itself when
+    no group is initialised)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes, steps, world, elapsed_max_ms):
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's
+    time (each replica runs the same step)."""
+    return world * step_bytes * steps / (elapsed_max_ms * 1e-3) / 1e9
+
+
 def algo_bytes(m, n, k, scale_group=16):
     """Packed FP4 weights + block scales + A + C bytes of one GEMM."""
     return n * k // 2 + n * k // scale_group + 2 * m * k + 2 * m * n
@@ -311,16 +328,12 @@ def run_ours(args, rank, world, local):
     per_kernel_ms = shape_durations(
         [[(lambda i=i, w=w: launch(i, w)) for w in (0, 1)] for i in range(len(SHAPES))],
         stream, max(3, min(args.steps // 8, 50)))
-    elapsed_max = elapsed_ms
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_max = float(t.item())
+    elapsed_max = max_over_ranks(elapsed_ms, dev)
 
     step_bytes = sum(algo_bytes(M_DECODE, n, k) for _, n, k in SHAPES)
     step_flops = sum(2 * M_DECODE * n * k for _, n, k in SHAPES)
     ms_per_step = elapsed_max / args.steps
-    value = world * step_bytes * args.steps / (elapsed_max * 1e-3) / 1e9
+    value = job_gbs(step_bytes, args.steps, world, elapsed_max)
     shapes = {}
     for i, (name, n, k) in enumerate(SHAPES):
         t = per_kernel_ms[i] * 1e-3
