@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--profile-m", type=int, default=M_DECODE)
     p.add_argument("--profile-fmt", choices=["nvfp4", "mxfp4", "nvfp4_f16"], default="nvfp4",
                    help="weight format / activation type of the --profile-only launches")
+    p.add_argument("--profile-moe", type=int, default=0, metavar="TOKENS",
+                   help="with --profile-only: one MXFP4 MoE grouped GEMM (8 experts, top-2, "
+                        "n=28672, k=4096) for TOKENS tokens instead of the four linears")
     return p.parse_args()
 
 
@@ -571,6 +574,22 @@ def run_profile_only(args, local):
     torch.cuda.set_device(dev)
     binding.load()
     ws = binding.Workspace(dev)
+    if args.profile_moe:
+        # the bench's MoE line: 8 experts, top-2 seeded routing, MXFP4 gate_up
+        E, n_e, k_e, tokens = 8, 28672, 4096, args.profile_moe
+        reps_e = []
+        for e in range(E):
+            w = synth.weights(n_e, k_e, seed=1000 + e, device=dev)
+            reps_e.append(binding.FP4Weight(w, "mxfp4").rep)
+            del w
+        rep = torch.cat(reps_e)
+        off = synth.moe_expert_offsets(tokens, E, 2, seed=tokens)
+        a = synth.activations(off[-1], k_e, seed=1100 + tokens, device=dev)
+        binding.moe_gemm(a, rep, off, n_e, "mxfp4", workspace=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        print(f"profile-only: MoE tokens={tokens} rows={off[-1]} launched 1 grouped GEMM", flush=True)
+        return
     m, fmt = args.profile_m, args.profile_fmt
     for i, (name, n, k) in enumerate(SHAPES):
         w = synth.weights(n, k, seed=100 + i, device=dev)
