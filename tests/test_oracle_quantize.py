@@ -61,7 +61,6 @@ def test_nvfp4_invariants(g):
     w = _weights(40, 512)
     if g == "amax":
         g = quantize.nvfp4_global_scale(w)
-        assert g == np.float32(np.float32(np.abs(w).max()) / np.float32(2688.0))
     g = np.float32(g)
     codes, sc = quantize.nvfp4_quantize(w, g)
     assert codes.shape == w.shape and sc.shape == (40, 512 // 16)
@@ -90,6 +89,19 @@ def test_nvfp4_invariants(g):
     # special cases: an all-zero block gets codes 0 and the smallest scale
     assert np.all(codes[0] == 0) and np.all(sc[0] == 0x01)
     assert np.all(codes[3] == 0)
+
+
+def test_nvfp4_global_scale_hand_worked():
+    """Values worked by hand in tests/golden/nvfp4_global_scale.txt."""
+    rows = read_golden("nvfp4_global_scale.txt")["_rows"]
+    assert len(rows) >= 5
+    for amax_txt, bits_txt in rows:
+        amax = float(amax_txt)
+        # a small row whose largest magnitude is |amax| (the entry keeps its sign)
+        w = np.array([[amax, 0.25 * amax, -0.5 * abs(amax), 0.0]], dtype=np.float32)
+        g = quantize.nvfp4_global_scale(w)
+        assert isinstance(g, np.float32), type(g)
+        assert int(np.asarray(g).view(np.uint32)) == int(bits_txt, 16), (amax, hex(int(np.asarray(g).view(np.uint32))))
 
 
 def test_nvfp4_exact_grid_block_and_saturation():
