@@ -5,15 +5,18 @@ a Llama-3-70B block (QKV 10240x8192, O 8192x8192, gate_up 57344x8192,
 down 8192x28672; W stored [n, k]) at decode size m = 16, NVFP4 weights with
 16-element E4M3 scales and global scale 1, A ~ N(0,1), W ~ N(0,0.02)
 (synthetic, seeded).  Weights are quantised and repacked offline (before the
-timed region).  Two weight copies (2 x 481 MB, far above the 129 MB L2) are
+timed region).  Two weight sets (2 x 481 MB, more than 3x the 129 MB L2) are
 used on alternate steps, so every weight byte comes from HBM.
 
 value = algorithmic bytes (packed weights + scales + A + C) of all steps on
 all ranks / max-over-ranks time, in GB/s.  A step is the four GEMM launches
 back to back on one stream (programmatic dependent launch lets each kernel's
-prologue overlap the previous one's tail; the host runs ahead of the GPU);
-CUDA events bracket the whole timed loop.  A second pass replays, per shape, a graph of consecutive
-launches of that shape to give its steady-state launch duration.
+prologue overlap the previous one's tail; the host runs ahead of the GPU).
+The headline is the median of 5 batches of `steps` steps, each batch
+bracketed by a barrier and a device synchronisation and timed with CUDA
+events.  Further passes replay, per shape, a graph of consecutive launches
+that rotate through R = max(2, ceil(3 L2 / weight bytes)) weight copies, to
+give each shape's steady-state launch duration.
 
 --impl reference times the FP64 CPU oracle (dequantise + GEMM) on a bounded
 sample of the same workload instead.
@@ -37,7 +40,7 @@ METRIC = "BF16×NVFP4 GEMM TFLOP/s & HBM GB/s (% roofline), Llama-3-70B shapes m
 SHAPES = [("qkv", 10240, 8192), ("o", 8192, 8192), ("gate_up", 57344, 8192), ("down", 8192, 28672)]
 M_DECODE = 16
 M_PREFILL = 256
-PAGE = 4096
+BATCHES = 5          # the headline is the median of this many timed batches
 
 
 def parse():
@@ -56,7 +59,19 @@ def parse():
     p.add_argument("--profile-moe", type=int, default=0, metavar="TOKENS",
                    help="with --profile-only: one MXFP4 MoE grouped GEMM (8 experts, top-2, "
                         "n=28672, k=4096) for TOKENS tokens instead of the four linears")
+    p.add_argument("--tile", default=os.environ.get("PETIT_CONFIG", ""), metavar="BN,KU",
+                   help="force the GEMM tile shape (activation rows per tile, 128-k chunks per "
+                        "unit) for every launch; default: the planner's choice (env PETIT_CONFIG)")
     return p.parse_args()
+
+
+def apply_tile(args, binding):
+    """Forward --tile / PETIT_CONFIG to the library; returns the forced pair."""
+    if not args.tile:
+        return None
+    bn, ku = (int(x) for x in args.tile.split(","))
+    binding.set_tile_config(bn, ku)
+    return [bn, ku]
 
 
 def dist_env():
@@ -123,54 +138,87 @@ def ncu_traffic(kernel_file):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples (200 ms period)."""
+    """nvidia-smi clock / throttle-reason samples (200 ms period), read by a
+    background thread as they arrive, each stamped with the host time."""
 
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
+        import threading
         self.proc = None
-        self.lines = []
+        self.rows = []            # (host time, sm MHz, max sm MHz, [reason flags])
+        self.lock = threading.Lock()
+        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(device_index), f"--query-gpu=timestamp,{self.Q}",
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            self.first.set()
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                row = (time.time(), float(parts[0]), float(parts[1]), parts[3:8])
+            except ValueError:
+                continue
+            with self.lock:
+                self.rows.append(row)
+            self.first.set()
+        self.first.set()
+
+    def wait_first(self, timeout=10.0):
+        """Block until the first sample has arrived (or nvidia-smi is gone)."""
+        self.first.wait(timeout)
 
     def stop(self):
         if self.proc is None:
             return
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        self.lines = [l for l in out.splitlines() if l.strip()]
+            self.proc.wait()
+        self.thread.join(timeout=5)
 
-    def summary(self, t0, t1):
-        import datetime
-        rows = []
-        for l in self.lines:
-            parts = [x.strip() for x in l.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
-            except ValueError:
-                continue
-        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+    def summary(self, windows):
+        """Median SM clock over the samples taken inside any of the (t0, t1)
+        host-time windows (all samples if none fell inside one), the largest
+        max clock, and the throttle reasons seen active."""
+        with self.lock:
+            rows = list(self.rows)
+        inside = [r for r in rows if any(t0 - 0.1 <= r[0] <= t1 + 0.1 for t0, t1 in windows)]
         use = inside if inside else rows
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_in_timed_region": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in use for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "period_ms": 200}
+
+
+def rotation_copies(weight_bytes, l2_bytes):
+    """Weight copies to rotate through so that each launch reads its weights
+    from HBM: R = max(2, ceil(3 * L2 / (W + S)))."""
+    return max(2, -(-3 * int(l2_bytes) // int(weight_bytes)))
+
+
+def l2_bytes(dev):
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
 
 
 # --------------------------------------------------------------------- oracle
@@ -238,18 +286,20 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------ GPU
-def shape_durations(launchers, stream, reps, burst=8):
-    """Steady-state duration (ms) of one launch of each shape: a graph holds
-    `burst` consecutive launches of that shape (alternating weight copies,
-    so programmatic dependent launch overlaps each prologue with the previous
-    kernel's tail, as inside a step) and is replayed `reps` times between two
-    stream events."""
+def shape_durations(launchers, stream, reps, min_burst=8):
+    """Steady-state duration (ms) of one launch of each shape.  launchers[i]
+    holds one launch function per weight copy of shape i; a graph holds at
+    least `min_burst` consecutive launches rotating through the copies (so
+    each launch reads its weights from HBM, and programmatic dependent launch
+    overlaps each prologue with the previous kernel's tail, as inside a step)
+    and is replayed `reps` times between two stream events."""
     out = []
     for fns in launchers:                      # fns[w]: launch with weight copy w
+        burst = len(fns) * max(1, -(-min_burst // len(fns)))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for b in range(burst):
-                fns[b & 1]()
+                fns[b % len(fns)]()
         for _ in range(2):
             g.replay()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -269,6 +319,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
+    tile = apply_tile(args, binding)
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)        # graphs are captured and replayed off the default stream
     torch.cuda.set_stream(stream)
@@ -307,31 +358,54 @@ def run_ours(args, rank, world, local):
         for i in range(len(SHAPES)):
             launch(i, s & 1)
 
+    l2 = l2_bytes(dev)
+
+    def rotated(reps, weight_bytes):
+        """`reps` extended by clones to the rotation count for its size."""
+        r = rotation_copies(weight_bytes, l2)
+        return list(reps) + [reps[0].clone() for _ in range(r - len(reps))]
+
+    # the clock sampler runs from before the warm-up to after the per-shape
+    # passes, and the timed region starts only once it has produced a sample
     sampler = ClockSampler(local)
+    sampler.wait_first()
+    windows = []
     for s in range(args.warmup):
         step(s)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    start.record(stream)
-    for s in range(args.steps):
-        step(s)
-    end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t_host1 = time.time()
-    sampler.stop()
-    clocks = sampler.summary(t_host0, t_host1)
-    elapsed_ms = start.elapsed_time(end)
-    # per-shape pass (after the timed region): steady-state launch durations
+    # the headline: BATCHES batches of `steps` steps each, every batch
+    # bracketed by a barrier and a device synchronisation and timed with CUDA
+    # events on the launching stream; the median batch (of the max over ranks)
+    # is reported
+    batch_ms = []
+    for _ in range(BATCHES):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        t_host0 = time.time()
+        start.record(stream)
+        for s in range(args.steps):
+            step(s)
+        end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        windows.append((t_host0, time.time()))
+        batch_ms.append(max_over_ranks(start.elapsed_time(end), dev))
+    elapsed_max = statistics.median(batch_ms)
+    # per-shape pass (after the timed region): steady-state launch durations,
+    # each shape rotating through enough weight copies to defeat L2
+    decode_reps = [rotated([sets[0][i].rep, sets[1][i]], n * k // 2 + n * k // 16)
+                   for i, (_, n, k) in enumerate(SHAPES)]
+
+    def launch_rep(i, rep):
+        binding.gemm(acts[i], rep, SHAPES[i][1], "nvfp4", 1.0, workspace=ws, out=outs[i])
+    t_shapes0 = time.time()
     per_kernel_ms = shape_durations(
-        [[(lambda i=i, w=w: launch(i, w)) for w in (0, 1)] for i in range(len(SHAPES))],
+        [[(lambda i=i, r=r: launch_rep(i, r)) for r in decode_reps[i]] for i in range(len(SHAPES))],
         stream, max(3, min(args.steps // 8, 50)))
-    elapsed_max = max_over_ranks(elapsed_ms, dev)
+    windows.append((t_shapes0, time.time()))
 
     step_bytes = sum(algo_bytes(M_DECODE, n, k) for _, n, k in SHAPES)
     step_flops = sum(2 * M_DECODE * n * k for _, n, k in SHAPES)
@@ -344,7 +418,9 @@ def run_ours(args, rank, world, local):
         shapes[name] = {"n": n, "k": k, "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1),
                         "tflops": round(2 * M_DECODE * n * k / t / 1e12, 2),
                         "weight_gbs": round((n * k // 2 + n * k // 16) / t / 1e9, 1),
-                        "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3)}
+                        "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3),
+                        "weight_copies": len(decode_reps[i])}
+    del decode_reps
     # the timed region holds only gemm_kernel<NVFP4, BN=16> launches (4 per
     # step), so its average launch duration is elapsed / launches
     launches = len(SHAPES) * args.steps
@@ -355,7 +431,7 @@ def run_ours(args, rank, world, local):
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": "gemm_kernel<NVFP4, BN=16, KU=2> (the only kernel in the timed region)",
                 "per_launch": "average algorithmic bytes of the 4 launches of a step / "
-                              "(timed-region time / launches)",
+                              "(median batch time / launches per batch)",
                 "avg_launch_us": round(avg_launch_s * 1e6, 3),
                 "peak_source": peaks["source"] + " hbm_gbs (copy bandwidth)"}
 
@@ -399,18 +475,18 @@ def run_ours(args, rank, world, local):
                    "copy of the step's activations and one device-to-host copy of its results; "
                    "preallocated device outputs; host synchronised every step"}
 
-    # prefill m = 256 (same kernels, tcgen05 N = 128 tiles), per-GEMM timing
+    # prefill m = 256 and the other per-shape lines: per-GEMM timing, each
+    # shape rotating through R weight copies
     def prepared(fmt, seed0, gscale):
-        """Two copies of the four weights in `fmt` (g = amax/(6*448) per
-        matrix if gscale), with their global scales."""
-        reps, gs = [[], []], []
+        """reps[i]: R copies of weight i in `fmt` (g = amax/(6*448) per matrix
+        if gscale), with the global scales."""
+        reps, gs = [], []
         for i, (name, n, k) in enumerate(SHAPES):
             w = synth.weights(n, k, seed=seed0 + i, device=dev)
             g = binding.nvfp4_global_scale(binding.absmax(w).item()) if gscale else 1.0
             fw = binding.FP4Weight(w, fmt, g)
             del w
-            reps[0].append(fw.rep)
-            reps[1].append(fw.rep.clone())
+            reps.append(rotated([fw.rep], fw.rep.numel()))
             gs.append(g)
         return reps, gs
 
@@ -420,14 +496,13 @@ def run_ours(args, rank, world, local):
              for i, (_, n, k) in enumerate(SHAPES)]
         c = [torch.empty((m, n), dtype=act, device=dev) for _, n, _ in SHAPES]
 
-        def fn(i, w):
-            binding.gemm(a[i], reps[w][i], SHAPES[i][1], fmt, gs[i], workspace=ws, out=c[i])
+        def fn(i, rep):
+            binding.gemm(a[i], rep, SHAPES[i][1], fmt, gs[i], workspace=ws, out=c[i])
         for i in range(len(SHAPES)):
             ws.ensure(binding.workspace_bytes(m, SHAPES[i][1], SHAPES[i][2], fmt))
-            for w in (0, 1):
-                fn(i, w)
+            fn(i, reps[i][0])
         torch.cuda.synchronize()
-        ms = shape_durations([[(lambda i=i, w=w: fn(i, w)) for w in (0, 1)] for i in range(len(SHAPES))],
+        ms = shape_durations([[(lambda i=i, r=r: fn(i, r)) for r in reps[i]] for i in range(len(SHAPES))],
                              stream, burst_reps)
         out = {}
         for i, (name, n, k) in enumerate(SHAPES):
@@ -436,7 +511,8 @@ def run_ours(args, rank, world, local):
             tf = 2 * m * n * k / t / 1e12
             out[name] = {"us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 2),
                          "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3),
-                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3),
+                         "weight_copies": len(reps[i])}
         out["step_us"] = round(float(ms.sum()) * 1e3, 2)
         return out
 
@@ -459,23 +535,23 @@ def run_ours(args, rank, world, local):
         reps_h, gs_h = prepared("nvfp4_f16", 650, False)
         fp16_decode = shape_table("nvfp4_f16", reps_h, gs_h, M_DECODE, 660)
         del reps_h
-        # NVFP4 m sweep at n = k = 8192 (two weight copies), and m = n = k = 4096
+        # NVFP4 m sweep at n = k = 8192, and m = n = k = 4096 (R weight copies)
         m_sweep = {}
         for (n, k, ms_list) in ((8192, 8192, (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)), (4096, 4096, (4096,))):
             wsq = synth.weights(n, k, seed=800 + n, device=dev)
             f0 = binding.FP4Weight(wsq, "nvfp4", 1.0)
             del wsq
-            r2 = [f0.rep, f0.rep.clone()]
+            rr = rotated([f0.rep], f0.rep.numel())
             for m in ms_list:
                 a = synth.activations(m, k, seed=900 + m, device=dev)
                 c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
                 ws.ensure(binding.workspace_bytes(m, n, k))
 
-                def fn(w, a=a, c=c, n=n):
-                    binding.gemm(a, r2[w], n, "nvfp4", 1.0, workspace=ws, out=c)
-                fn(0); fn(1)
+                def fn(rep, a=a, c=c, n=n):
+                    binding.gemm(a, rep, n, "nvfp4", 1.0, workspace=ws, out=c)
+                fn(rr[0])
                 torch.cuda.synchronize()
-                t = float(shape_durations([[lambda: fn(0), lambda: fn(1)]], stream, 10)[0]) * 1e-3
+                t = float(shape_durations([[lambda r=r: fn(r) for r in rr]], stream, 10)[0]) * 1e-3
                 b = algo_bytes(m, n, k)
                 tf = 2 * m * n * k / t / 1e12
                 roof_t = max(b / (peaks["hbm_gbs"] * 1e9), 2 * m * n * k / (peaks["bf16_tflops"] * 1e12))
@@ -483,14 +559,15 @@ def run_ours(args, rank, world, local):
                     "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 1),
                     "bound": "hbm" if b / (peaks["hbm_gbs"] * 1e9) >= 2 * m * n * k / (peaks["bf16_tflops"] * 1e12)
                     else "tensor",
-                    "frac_roofline": round(roof_t / t, 3)}
-            del f0, r2
+                    "frac_roofline": round(roof_t / t, 3), "weight_copies": len(rr)}
+            del f0, rr
         # MoE grouped GEMM: 8 experts, top-2, Mixtral-8x7B-like gate_up
         # (n = 28672, k = 4096), MXFP4, seeded Zipf-like routing
         moe = {}
         E, n_e, k_e = 8, 28672, 4096
         ew = []
-        for c in (0, 1):
+        n_sets = rotation_copies(E * n_e * k_e * 17 // 32, l2)
+        for c in range(n_sets):
             reps_e = []
             for e in range(E):
                 w = synth.weights(n_e, k_e, seed=1000 + 10 * c + e, device=dev)
@@ -505,35 +582,38 @@ def run_ours(args, rank, world, local):
 
             def fn(w, a=a, cm=cm, off=off):
                 binding.moe_gemm(a, ew[w], off, n_e, "mxfp4", workspace=ws, out=cm)
-            fn(0); fn(1)
+            fn(0)
             torch.cuda.synchronize()
-            t = float(shape_durations([[lambda: fn(0), lambda: fn(1)]], stream, 10)[0]) * 1e-3
+            t = float(shape_durations([[lambda w=w: fn(w) for w in range(n_sets)]], stream, 10)[0]) * 1e-3
             active = sum(1 for e in range(E) if off[e + 1] > off[e])
             b = active * n_e * k_e * 17 // 32 + 2 * off[-1] * (k_e + n_e)
             tf = 2 * off[-1] * n_e * k_e / t / 1e12
             moe[f"tokens={tokens} top2 rows={off[-1]}"] = {
                 "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "tflops": round(tf, 1),
                 "frac_hbm": round(b / t / 1e9 / peaks["hbm_gbs"], 3), "active_experts": active,
-                "expert_rows": [off[e + 1] - off[e] for e in range(E)]}
+                "expert_rows": [off[e + 1] - off[e] for e in range(E)], "weight_copies": n_sets}
         del ew
         # context row: cuBLAS BF16 dense GEMM on the same shapes (BF16 weights are
-        # 3.6x the NVFP4 bytes; two copies alternate so they come from HBM too)
+        # 3.6x the NVFP4 bytes; R copies rotate so they come from HBM too)
         cublas = {}
         for i, (name, n, k) in enumerate(SHAPES):
-            wb = [synth.weights(n, k, seed=950 + i + 10 * c, device=dev) for c in (0, 1)]
+            wb = [synth.weights(n, k, seed=950 + i + 10 * c, device=dev)
+                  for c in range(rotation_copies(2 * n * k, l2))]
             row = {}
             for m in (M_DECODE, M_PREFILL):
                 a = synth.activations(m, k, seed=960 + m, device=dev)
-                fns = [lambda c=c, a=a: torch.matmul(a, wb[c].t()) for c in (0, 1)]
-                for f in fns:
-                    f()
+                fns = [lambda c=c, a=a: torch.matmul(a, wb[c].t()) for c in range(len(wb))]
+                fns[0]()
                 torch.cuda.synchronize()
                 t = float(shape_durations([fns], stream, 10)[0]) * 1e-3
                 ours = (per_kernel_ms[i] * 1e-3) if m == M_DECODE else prefill[name]["us"] * 1e-6
                 row[f"m={m}"] = {"us": round(t * 1e6, 2), "tflops": round(2 * m * n * k / t / 1e12, 1),
-                                 "ours_speedup": round(t / ours, 2)}
+                                 "ours_speedup": round(t / ours, 2), "weight_copies": len(wb)}
             cublas[name] = row
             del wb
+
+    sampler.stop()
+    clocks = sampler.summary(windows)
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -553,11 +633,16 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights quantised to NVFP4 on the GPU)",
-            "config": dict(decode_config(world),
-                           l2="2 rotating weight sets of 481 MB each (> 129 MB L2)"),
+            "config": dict(decode_config(world), tile_override=tile,
+                           l2="2 rotating weight sets of 481 MB each (> 3x the L2); per-shape lines "
+                              "rotate R = max(2, ceil(3 L2 / weight bytes)) copies"),
+            "timing": f"median of {BATCHES} batches of `steps` steps; each batch bracketed by a barrier and "
+                      "a device synchronisation, CUDA events on the launching stream",
+            "batch_ms": [round(b, 4) for b in batch_ms],
             "tflops": round(world * step_flops * args.steps / (elapsed_max * 1e-3) / 1e12, 2),
             "shapes": shapes, "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
-            "gpu_launches": len(SHAPES) * args.steps, "clocks": clocks,
+            "gpu_launches": BATCHES * len(SHAPES) * args.steps,
+            "gpu_launches_per_batch": len(SHAPES) * args.steps, "clocks": clocks,
             "prefill_m256": prefill, "mxfp4_decode": mxfp4, "fp16_decode_m16": fp16_decode,
             "m_sweep": m_sweep,
             "moe_mxfp4_gate_up": moe, "cublas_bf16_context": cublas,
@@ -573,6 +658,7 @@ def run_profile_only(args, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
+    apply_tile(args, binding)
     ws = binding.Workspace(dev)
     if args.profile_moe:
         # the bench's MoE line: 8 experts, top-2 seeded routing, MXFP4 gate_up

@@ -68,7 +68,8 @@ SIGNATURES = {
                                                  _c_sz, _c_p]),
     "petit_moe_gemm_bf16_nvfp4": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_i64,
                                                  _c_p, _c_sz, _c_p]),
-    "petit_get_device_status": (ctypes.c_int, [_c_p, _c_p]),
+    "petit_get_device_status": (ctypes.c_int, [_c_p, _c_sz, _c_p]),
+    "petit_set_tile_config": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
 }
 
@@ -204,7 +205,7 @@ class Workspace:
 
     def status(self):
         """PETIT_OK (0) or the error the kernels recorded (clears it)."""
-        return load().petit_get_device_status(_ptr(self.buf), _stream())
+        return load().petit_get_device_status(_ptr(self.buf), self.buf.numel(), _stream())
 
 
 def gemm(A, rep, n, fmt="nvfp4", global_scale=1.0, workspace=None, out=None):
@@ -266,6 +267,13 @@ def moe_gemm(A, rep, expert_offsets, n, fmt="mxfp4", global_scales=None, workspa
                                          buf.numel(), _stream())
     _check(st, "moe_gemm_" + fmt)
     return C
+
+
+def set_tile_config(bn=0, ku=0):
+    """Force the GEMM tile shape (bn activation rows, ku 128-k chunks per
+    unit) for later calls in this process; (0, 0) restores the planner."""
+    _check(load().petit_set_tile_config(int(bn), int(ku)), "set_tile_config")
+    workspace_bytes.cache_clear()
 
 
 def selftest_timeout(workspace, timeout_us=1000):

@@ -349,8 +349,13 @@ petit_status_t petit_gemm_bf16_mxfp4(const void* A, const uint8_t* rep, void* C,
   return gemm_common(kMXFP4, A, rep, 1.0f, C, m, n, k, workspace, workspace_bytes, stream);
 }
 
-petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream) {
-  if (!workspace) return PETIT_ERR_INVALID_ARG;
+petit_status_t petit_set_tile_config(int bn, int ku) {
+  return petit::set_tile_override(bn, ku) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
+}
+
+petit_status_t petit_get_device_status(void* workspace, size_t workspace_bytes,
+                                       petit_stream_t stream) {
+  if (!workspace || workspace_bytes < petit::kWsHeaderBytes) return PETIT_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return PETIT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return PETIT_ERR_CUDA;
@@ -358,7 +363,13 @@ petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream) {
   if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return PETIT_ERR_CUDA;
   if (word == 0) return PETIT_OK;
-  if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return PETIT_ERR_CUDA;
+  // A kernel that stopped early may have left split-tile arrival counters
+  // raised (CTAs that had arrived before the abort); clear them with the
+  // status word so the next call on this workspace starts from zero.
+  const size_t counters_end = petit::kWsHeaderBytes + petit::kWsCountersBytes;
+  const size_t clear = workspace_bytes >= counters_end ? counters_end : sizeof(word);
+  if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return PETIT_ERR_CUDA;
   return (word & petit::kStatusTimeout) ? PETIT_ERR_TIMEOUT : PETIT_ERR_CUDA;
 }
 
@@ -378,11 +389,10 @@ petit_status_t petit_selftest_timeout(void* workspace, size_t workspace_bytes, u
 // ---------------------------------------------------------------------------
 // GEMM without a caller-provided workspace.
 //
-// Some callers cannot allocate device memory when they call the GEMM: code
-// running while a CUDA graph is being captured (cudaMalloc is not a stream
-// operation), plug-ins whose host framework owns all device memory and
-// forbids allocation inside their enqueue call, and latency-critical serving
-// loops where cudaMalloc's implicit device synchronisation is unacceptable.
+// Some callers cannot allocate device memory when they call the GEMM:
+// plug-ins whose host framework owns all device memory and forbids
+// allocation inside their enqueue call, and latency-critical serving loops
+// where cudaMalloc's implicit device synchronisation is unacceptable.
 // For them the split-K scratch (status word, arrival counters, FP32 partial
 // sums) lives in a fixed array in this library's device image instead of a
 // caller buffer.
@@ -418,7 +428,9 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
   {
     // first call on a device (with that device current): look up the
     // array's device address -- in host code its name is only a host-side
-    // stand-in, never a device address
+    // stand-in, never a device address.  The address is kept for the life of
+    // the process; cudaDeviceReset unloads the module and makes it stale, so
+    // this entry point must not be used after a reset of that device.
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
       void* p = nullptr;
@@ -430,13 +442,14 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
     }
     scratch = g_noalloc_ptr[dev];
   }
+  // every check that can fail comes before the first enqueue
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the arrival counters must start at zero; the array
   // keeps whatever the previous call left in it
   if (cudaMemsetAsync(scratch, 0, plan.ws.partials_off, s) != cudaSuccess) return PETIT_ERR_CUDA;
-  CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
   petit::GemmArgs args{A, rep, C, m, n, k, global_scale * 256.0f, static_cast<uint8_t*>(scratch),
                        kGemmTimeoutNs};
   return from_cuda(petit::launch_gemm(plan, args, map, s));

@@ -33,6 +33,8 @@
 //   the FP4 chunk and the activation tile.
 // * Every wait is bounded; a wait that runs out records a timeout in the
 //   workspace status word and the CTA shuts down cleanly.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -188,6 +190,13 @@ struct Cfg {
                     kNumA % kMmaThreads == 0 && kNumA <= kXStages,
                 "fixed consumer per barrier");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  // tcgen05.alloc of all 512 tensor-memory columns blocks (in hardware, with
+  // no time limit) until the columns are free.  It never waits here because
+  // no two CTAs of this kernel fit on one SM: each takes more than half of
+  // the SM's 228 KB of shared memory, so the next launch's CTA (under
+  // programmatic dependent launch) starts on an SM only after this one has
+  // exited and freed its columns.
+  static_assert(2 * kSmemBytes > 228 * 1024, "one CTA per SM");
   // barriers, tensor-memory holder, flags and the deferred fix-up job fit in
   // the 1024 bytes after the rings
   static_assert((2 * kWStages + 2 * kXStages + kNumA + 2 * kNumD + kMaxMmaThreads + 1) * 8 + 16 +
@@ -794,7 +803,23 @@ cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tma
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+std::atomic<int> g_tile_override{0};   // bn | ku << 16, or 0: the planner decides
+
 }  // namespace
+
+int tile_override() { return g_tile_override.load(std::memory_order_relaxed); }
+
+bool set_tile_override(int bn, int ku) {
+  if (bn == 0 && ku == 0) {
+    g_tile_override.store(0);
+    return true;
+  }
+  if ((bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) || (ku != 1 && ku != 2) ||
+      (ku == 2 && bn > 64))
+    return false;
+  g_tile_override.store(bn | (ku << 16));
+  return true;
+}
 
 GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
                       int num_sms) {
@@ -832,6 +857,13 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
   }
   // two chunks per unit halves the copy requests when the A tile is small
   pl.ku = (pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
+  const int ov = tile_override();
+  if (ov != 0) {
+    // a forced tile shape (tuning and tests): BN as given, two chunks per
+    // unit only where that kernel exists and k holds an even number of them
+    pl.bn = ov & 0xFFFF;
+    pl.ku = ((ov >> 16) == 2 && pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
+  }
   pl.n_tiles = static_cast<int>(n / kTileN);
   pl.k_stages = static_cast<int>(k / kStageK);
   int64_t tiles = 0;

@@ -49,6 +49,11 @@ struct GemmPlan {
 };
 
 GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
+// Process-wide forced tile shape for the planner (tuning and tests): bn in
+// {16, 32, 64, 128, 256}, ku in {1, 2} (2 only for bn <= 64); (0, 0) clears.
+// Returns false for any other pair.
+bool set_tile_override(int bn, int ku);
+int tile_override();   // bn | ku << 16, or 0
 // row_off: num_groups + 1 non-decreasing offsets starting at 0
 GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
                       int num_sms);

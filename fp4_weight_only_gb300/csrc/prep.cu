@@ -13,10 +13,18 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Blocks for a grid-stride kernel over `work` items: one item per thread, at
+// most 32 blocks per SM of the current device (the kernels loop beyond that).
 int grid_for(int64_t work, int per_block = kThreads) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    sms = 1;
+  }
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
-  if (g > 152 * 32) g = 152 * 32;
+  if (g > static_cast<int64_t>(sms) * 32) g = static_cast<int64_t>(sms) * 32;
   return static_cast<int>(g);
 }
 

@@ -245,18 +245,25 @@ petit_status_t petit_moe_gemm_bf16_nvfp4(const void* A, const uint8_t* rep,
 
 /* NVFP4 GEMM without a workspace argument.  The pages have no counterpart to
  * this entry point; it is for callers that cannot allocate device memory at
- * the time they call the GEMM: code running while a CUDA graph is being
- * captured, plug-ins whose host framework owns all device memory, and
+ * the time they call the GEMM: plug-ins whose host framework owns all device
+ * memory and forbids allocation inside their enqueue call, and
  * latency-critical loops that cannot afford cudaMalloc's implicit device
  * synchronisation.  It computes what petit_gemm_bf16_nvfp4 computes, but its
  * split-K scratch is an 8 MiB array built into the library's device image:
  * every GPU that loads the library holds those 8 MiB until the process
  * exits, and the call itself allocates and frees nothing.
- *   - Problems whose scratch does not fit (on a 152-SM GB300: m > 32, for any
- *     n, k) are rejected with PETIT_ERR_WORKSPACE; use the workspace entry
- *     point for them.
+ *   - The scratch a problem needs is 4352 + 1024 * ctas * bn bytes, where
+ *     ctas = min(work units, SMs) and bn is the planner's activation tile
+ *     height (16, 32, 64, 128 or 256 for m up to 16, 32, 64, 128, above).
+ *     Problems whose scratch exceeds 8 MiB are rejected with
+ *     PETIT_ERR_WORKSPACE (use the workspace entry point for them); when the
+ *     grid fills all 152 SMs of a GB300, as on the Llama-3-70B shapes, that
+ *     accepts m <= 32.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process; make
+ *     that first call before any stream capture.  cudaDeviceReset makes the
+ *     kept address stale: do not use this entry point on a device after
+ *     resetting it.
  *   - Each call clears the scratch's status word and counters on `stream`
  *     before its kernel.  All calls on a device share the one array, so calls
  *     whose execution overlaps on the GPU (different streams, concurrent
@@ -269,12 +276,31 @@ petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uint8_t* rep,
                                              int64_t m, int64_t n, int64_t k,
                                              petit_stream_t stream);
 
+/* ------------------------------------------------------------------ tuning */
+
+/* Forces the tile shape of every later GEMM plan in this process, for tile
+ * tuning and tests (Petit PyPI page, "Known limitations": tile parameters may
+ * need tuning for a given matrix size): bn activation rows per tile (the MMA
+ * N side: 16, 32, 64, 128 or 256) and ku 128-k chunks per pipeline unit (1,
+ * or 2 for bn <= 64; a problem whose k holds an odd number of 128-k chunks
+ * runs with 1).  bn = ku = 0 gives the choice back to the planner.  The
+ * workspace size queries follow the forced shape, so query them after this
+ * call.  Not thread-safe with respect to GEMM calls running concurrently on
+ * other host threads.  Errors: PETIT_ERR_INVALID_ARG for any other pair. */
+petit_status_t petit_set_tile_config(int bn, int ku);
+
 /* --------------------------------------------------------- error reporting */
 
-/* Waits for `stream`, reads the status word the kernels keep at the start of
- * `workspace` and clears it.  Returns PETIT_OK, PETIT_ERR_TIMEOUT (a bounded
- * wait ran out in some earlier call on this workspace) or PETIT_ERR_CUDA. */
-petit_status_t petit_get_device_status(void* workspace, petit_stream_t stream);
+/* Waits for `stream`, then reads the status word the kernels keep at the
+ * start of `workspace` (device, workspace_bytes >= 256).  Returns PETIT_OK,
+ * PETIT_ERR_TIMEOUT (a bounded wait ran out in some earlier call on this
+ * workspace) or PETIT_ERR_CUDA.  When the word is not zero it is cleared,
+ * together with the split-tile arrival counters (bytes 256..4351, when
+ * workspace_bytes covers them) that a kernel which stopped early may have
+ * left raised; the workspace can then be used again without re-zeroing it.
+ * This call synchronises the stream. */
+petit_status_t petit_get_device_status(void* workspace, size_t workspace_bytes,
+                                       petit_stream_t stream);
 
 /* Fault-detection self test: launches one CTA that waits on a barrier nobody
  * arrives at, with a limit of `timeout_us` microseconds (1..10^6).  The wait

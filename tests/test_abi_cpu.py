@@ -77,7 +77,8 @@ def test_argument_validation_without_gpu(lib):
     assert lib.petit_absmax_bf16(a, 0, a, s) == 1
     assert lib.petit_selftest_timeout(a, 16, 100, s) == 4
     assert lib.petit_selftest_timeout(a, 256, 0, s) == 1
-    assert lib.petit_get_device_status(NULL, s) == 1
+    assert lib.petit_get_device_status(NULL, 4608, s) == 1
+    assert lib.petit_get_device_status(a, 16, s) == 1
     # sizes are 0 for invalid shapes
     assert lib.petit_gemm_workspace_bytes(16, 1000, 1024, 0) == 0
     assert lib.petit_gemm_workspace_bytes(0, 1024, 1024, 0) == 0
@@ -91,3 +92,11 @@ def test_no_device_is_reported_not_crashed(lib):
     # valid arguments, but no usable device: a CUDA error status, never a crash
     assert lib.petit_gemm_bf16_nvfp4(a, a, 1.0, a, 16, 1024, 1024, a, 1 << 30, P(0)) == 6
     assert lib.petit_gemm_workspace_bytes(16, 1024, 1024, 0) == 0
+
+
+def test_tile_config_override_validation(lib):
+    assert lib.petit_set_tile_config(48, 1) == 1
+    assert lib.petit_set_tile_config(128, 2) == 1
+    assert lib.petit_set_tile_config(16, 3) == 1
+    assert lib.petit_set_tile_config(256, 1) == 0
+    assert lib.petit_set_tile_config(0, 0) == 0

@@ -6,7 +6,7 @@ same binding call as the bench; the oracle checks sampled output columns
 is row-local, so the sampled rows' codes do not depend on the other rows):
 
 * NVFP4 decode, m = 16, the four Llama-3-70B linears (g = 1);
-* MXFP4 decode, m in {1, 4, 8, 16}, same shapes;
+* MXFP4 decode, m in {1, 4, 8, 16}, and MXFP4 at m = 256, same shapes;
 * NVFP4 prefill, m = 256, activations with 0.1 % N(0, 20) outliers and the
   per-tensor global scale g = amax / (6 * 448);
 * NVFP4 m sweep 1 .. 1024 at n = k = 8192, and m = n = k = 4096.
@@ -65,6 +65,17 @@ def test_mxfp4_decode_llama(cuda_lib, name, nk):
     for m in (1, 4, 8, 16):
         a = synth.activations(m, k, seed=202 + m)
         _check(cuda_lib, w, rep, a, "mxfp4", 1.0, f"{name} m={m}")
+
+
+@pytest.mark.parametrize("name,nk", SHAPES)
+def test_mxfp4_prefill_llama_m256(cuda_lib, name, nk):
+    """MXFP4 at m = 256 (the prefill size bench.py also reports for MXFP4):
+    gate_up and down run 256-row activation tiles, QKV and O two 128-row
+    tiles."""
+    n, k = nk
+    w, rep = _prepare(cuda_lib, n, k, "mxfp4", seed=106)
+    a = synth.activations(256, k, seed=206, outlier_frac=0.001, outlier_std=20.0)
+    _check(cuda_lib, w, rep, a, "mxfp4", 1.0, f"{name} mxfp4 m=256")
 
 
 @pytest.mark.parametrize("name,nk", SHAPES)

@@ -154,6 +154,45 @@ def test_bounded_wait_reports_timeout(cuda_lib):
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), "after timeout")
 
 
+@pytest.mark.parametrize("bn,ku", [(16, 1), (16, 2), (32, 1), (32, 2), (64, 1), (64, 2), (128, 1), (256, 1)])
+def test_forced_tile_config(cuda_lib, bn, ku):
+    """Every (BN, KU) kernel forced on one problem: m = 70 spans several
+    16/32/64-row tiles and a ragged tail; k = 2048 gives split tiles."""
+    n, k, m = 512, 2048, 70
+    w = synth.weights(n, k, seed=90)
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
+    a = synth.activations(m, k, seed=91)
+    cuda_lib.set_tile_config(bn, ku)
+    try:
+        c = _gemm(cuda_lib, a.cuda(), rep, n, "nvfp4", 1.0)
+    finally:
+        cuda_lib.set_tile_config(0, 0)
+    assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), f"bn={bn} ku={ku}")
+
+
+def test_timeout_recovery_clears_arrival_counters(cuda_lib):
+    """A kernel that stops early on a timeout can leave split-tile arrival
+    counters raised.  Reading the status clears them with the status word, so
+    the next split-K GEMM on the same workspace is correct again.  The
+    aborted state is made on the host: status word = timeout, every counter
+    dirty."""
+    n, k, m = 1024, 8192, 16          # 256 units over the SMs: many split tiles
+    w = synth.weights(n, k, seed=19)
+    codes, scales, rep = _prep(cuda_lib, w, "nvfp4")
+    a = synth.activations(m, k, seed=19)
+    ws = cuda_lib.Workspace()
+    buf = ws.ensure(cuda_lib.workspace_bytes(m, n, k))
+    words = buf[:4352].view(torch.int32)
+    words[0] = 1                        # the timeout bit
+    words[64:].fill_(3)                 # counters region [256, 4352)
+    torch.cuda.synchronize()
+    assert ws.status() == 7
+    assert int(buf[:4352].count_nonzero()) == 0
+    c = cuda_lib.gemm(a.cuda(), rep, n, "nvfp4", workspace=ws)
+    assert ws.status() == 0
+    assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), "after recovery")
+
+
 # m -> the kernel's activation tile N (16/32/64/128/256) and chunks per unit;
 # k/128 odd forces one chunk per unit.  Repeated launches catch pipeline
 # races (a lost or aliased barrier phase shows up as a timeout status or a
