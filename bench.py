@@ -333,6 +333,7 @@ def run_ours(args, rank, world, local):
         del w
         sets[0].append(fw)
         sets[1].append(fw.rep.clone())
+        torch.cuda.synchronize()
         acts.append(synth.activations(M_DECODE, k, seed=200 + i, device=dev))
         outs.append(torch.empty((M_DECODE, n), dtype=torch.bfloat16, device=dev))
     ws = binding.Workspace(dev)
@@ -363,7 +364,11 @@ def run_ours(args, rank, world, local):
     def rotated(reps, weight_bytes):
         """`reps` extended by clones to the rotation count for its size."""
         r = rotation_copies(weight_bytes, l2)
-        return list(reps) + [reps[0].clone() for _ in range(r - len(reps))]
+        out = list(reps) + [reps[0].clone() for _ in range(r - len(reps))]
+        # a GEMM reads its weights while the previous kernel is finishing:
+        # the copies must be complete before the first launch that reads them
+        torch.cuda.synchronize()
+        return out
 
     # the clock sampler runs from before the warm-up to after the per-shape
     # passes, and the timed region starts only once it has produced a sample
@@ -575,6 +580,7 @@ def run_ours(args, rank, world, local):
                 del w
             ew.append(torch.cat(reps_e))
             del reps_e
+        torch.cuda.synchronize()   # the concatenated weights are complete before any GEMM reads them
         for tokens in (16, 256):
             off = synth.moe_expert_offsets(tokens, E, 2, seed=tokens)
             a = synth.activations(off[-1], k_e, seed=1100 + tokens, device=dev)
@@ -669,6 +675,7 @@ def run_profile_only(args, local):
             reps_e.append(binding.FP4Weight(w, "mxfp4").rep)
             del w
         rep = torch.cat(reps_e)
+        torch.cuda.synchronize()   # complete before the GEMM reads it
         off = synth.moe_expert_offsets(tokens, E, 2, seed=tokens)
         a = synth.activations(off[-1], k_e, seed=1100 + tokens, device=dev)
         binding.moe_gemm(a, rep, off, n_e, "mxfp4", workspace=ws)

@@ -284,39 +284,25 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmap_a);
-    // Weights are never written by the preceding kernel, and L2 is the
-    // device's point of coherence, so the first ring's worth of this CTA's
-    // weight chunks can be pulled into L2 before the grid dependency wait
-    // (while the previous kernel finishes); the copies after the wait then
-    // hit L2.
-    const int64_t tile0 = u0 / KS;
-    int64_t ku = u0 - tile0 * KS;
-    TileCursor cur = cursor_at<BN>(p, tile0);
-    for (int64_t u = u0; u < u1 && u < u0 + C::kWStages; ++u) {
-      bulk_prefetch_l2(p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, ku * KU, KS * KU),
-                       C::kWBytes);
-      if (++ku == KS) {
-        ku = 0;
-        cursor_next<BN>(p, cur);
-      }
-    }
-  }
+  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap_a);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // Programmatic dependent launch: the prologue above may overlap the tail of
-  // the previous kernel on the stream; nothing below touches global memory
-  // before that kernel has completed (its outputs may be A, or the weights).
-  grid_dependency_wait();
+  // Programmatic dependent launch.  The next kernel on the stream may begin
+  // launching now; its CTAs take an SM only when this kernel's CTA on it has
+  // exited (shared memory), so they never crowd out this grid.  Before the
+  // grid dependency wait this kernel touches only its weights, which must not
+  // be written by the kernel just before it on the stream (a documented
+  // precondition): the first ring of weight chunks is copied and the first
+  // units are dequantised into tensor memory while the previous kernel
+  // finishes.  The threads that read activations or the device-resident
+  // global scale, or write global memory, wait first.
   grid_launch_dependents();
 
-  auto fail = [&]() {
-    atomicOr(p.status, kStatusTimeout);
-    *abort_flag = 1;
-  };
+  // a wait that runs out records the abort in shared memory only; thread 0
+  // (which has passed the grid dependency wait) reports it at the end
+  auto fail = [&]() { *abort_flag = 1; };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (mbar_wait_bounded(smem_u32(bar), parity, p.timeout_ns, abort_flag)) return true;
     if (!*abort_flag) fail();
@@ -352,26 +338,33 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const uint32_t wfree0 = smem_u32(&wfree[0]), wfull0 = smem_u32(&wfull[0]);
       const uint32_t mdone0 = smem_u32(&mdone[0]), xfull0 = smem_u32(&xfull[0]);
       uint32_t wdst = wdst0, xdst = xdst0, wbar = 0, xbar = 0;   // bar: stage * 8
+      auto issue_weights = [&]() {
+        mbar_arrive_expect_tx(wfull0 + wbar, C::kWBytes);
+        bulk_g2s(wdst, wsrc, C::kWBytes, wfull0 + wbar, policy);
+        ++wi;
+        wsrc += C::kWBytes;
+        wdst += C::kWBytes;
+        wbar += 8;
+        if (wbar == 8 * C::kWStages) {
+          wbar = 0;
+          wdst = wdst0;
+          wph ^= 1u;
+        }
+        if (++w_ku == KS) {
+          w_ku = 0;
+          cursor_next<BN>(p, wc);
+          wsrc = p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, 0, KS * KU);
+        }
+      };
+      // the first ring of weight chunks goes out before the grid dependency
+      // wait (every stage starts free)
+      while (wi < nu && wi < C::kWStages) issue_weights();
+      grid_dependency_wait();
       const uint64_t t0 = global_timer_ns();
       for (uint32_t spin = 0; wi < nu || xi < nu;) {
         bool progress = false;
         if (wi < nu && mbar_test_wait(wfree0 + wbar, wph ^ 1u)) {
-          mbar_arrive_expect_tx(wfull0 + wbar, C::kWBytes);
-          bulk_g2s(wdst, wsrc, C::kWBytes, wfull0 + wbar, policy);
-          ++wi;
-          wsrc += C::kWBytes;
-          wdst += C::kWBytes;
-          wbar += 8;
-          if (wbar == 8 * C::kWStages) {
-            wbar = 0;
-            wdst = wdst0;
-            wph ^= 1u;
-          }
-          if (++w_ku == KS) {
-            w_ku = 0;
-            cursor_next<BN>(p, wc);
-            wsrc = p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, 0, KS * KU);
-          }
+          issue_weights();
           progress = true;
         }
         if (xi < nu && mbar_test_wait(mdone0 + xbar, xph ^ 1u)) {
@@ -480,6 +473,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
     int64_t seg = 0;
     const int64_t first_tile_of_cta = u0 / KS;
+    // C, the partials and the counters may be in use by the previous kernel
+    // on the stream until it has completed
+    grid_dependency_wait();
     // epilogue factor: a device-resident global scale is read here, after the
     // grid dependency wait, so a preceding kernel may have produced it
     const float alpha_dev = p.alpha_dev ? p.alpha_scale * *p.alpha_dev : 0.0f;
@@ -705,6 +701,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  // a wait that ran out anywhere in the CTA is reported by thread 0, which
+  // has passed the grid dependency wait
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
 
   // Deferred fix-up of the last segment's tile (see FixJob), by all threads:
   // element e = activation row * 128 + weight row, as in a partial slot, so

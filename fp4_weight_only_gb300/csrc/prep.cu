@@ -200,6 +200,11 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
       *reinterpret_cast<uint16_t*>(sdst + i * 2) = *reinterpret_cast<const uint16_t*>(src);
     }
   }
+  // The GEMM reads its weights before its grid dependency wait, so it may
+  // start (right after this kernel's CTAs exit) without the usual end-of-
+  // kernel flush: make this thread's writes visible device-wide before it
+  // exits, so a GEMM may directly follow the repack on the same stream.
+  __threadfence();
 }
 
 // ------------------------------------------------------------- dequant hook

@@ -34,6 +34,17 @@
  *     returns a non-zero petit_status_t and enqueues nothing.  No entry point
  *     aborts, throws or prints.
  *   - Device pointers must be 16-byte aligned (PETIT_ERR_MISALIGNED).
+ *   - Repacked weights are read-only inputs that must not change while GEMMs
+ *     that read them are in flight.  Every GEMM kernel is launched with
+ *     programmatic dependent launch and starts copying and dequantising its
+ *     weights while the kernel before it on the stream is still finishing
+ *     (it reads activations and the device global scale, and writes any
+ *     output, only after that kernel has completed).  So the kernel enqueued
+ *     just before a GEMM on the same stream must not write that GEMM's `rep`
+ *     buffer: after copying or modifying weights, synchronise or enqueue
+ *     other work before the first GEMM that reads them.  The repack kernels
+ *     of this library are the exception: they make their output visible
+ *     before they exit, so a GEMM may follow petit_repack_* directly.
  *   - The device must be compute capability 10.3 (GB300, sm_103a)
  *     (PETIT_ERR_ARCH).
  */

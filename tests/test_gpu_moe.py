@@ -31,7 +31,11 @@ def _experts(cuda_lib, E, n, k, fmt, seed, device_quant=False):
         reps.append(cuda_lib.repack(wp, sp, fmt))
         ws_cpu.append(w)
         gs.append(g)
-    return torch.cat(reps), ws_cpu, gs
+    rep = torch.cat(reps)
+    # a GEMM reads its weights while the kernel before it on the stream is
+    # still finishing, so the copy that wrote them must have completed
+    torch.cuda.synchronize()
+    return rep, ws_cpu, gs
 
 
 def _check(cuda_lib, c, a, ws_cpu, gs, off, fmt, rows=None):
