@@ -75,16 +75,26 @@ struct Params {
   float group_alpha[kMaxGroups];      // epilogue factor per group
 };
 
-// The split-tile fix-up of a CTA's last segment, when this CTA arrives last
-// on that tile.  It is deferred to after the kernel's final barrier so that
-// every warp shares it: with BN = 256 the tile's partials are 128 KB per
-// contributor, which the four epilogue warps alone would sum in sixteen
-// dependent 16-column rounds at the end of the kernel.
+// Split tiles.  A contributor stores its FP32 partial and then arrives on
+// the tile's counter (acq_rel); the last to arrive adds all partials in CTA
+// order and writes C, so the result is the same whichever CTA sums, and no
+// CTA ever waits for another.  A CTA's last segment is usually the
+// beginning of a tile whose other contributors ran their parts at the start
+// of their ranges: if the counter (an acquire load, before and again after
+// the segment's MMAs) already shows every other contributor, this CTA is
+// the last one without arriving, so it stores nothing and adds its
+// accumulator straight from tensor memory.
+//
+// When the summed tile is the CTA's last segment the sum is deferred to
+// after the kernel's final barrier, so that every warp shares it: with
+// BN = 256 the tile's partials are 128 KB per contributor.
 struct FixJob {
   uint16_t* c_g;                        // output rows of the tile's group
   int64_t c_first, c_last, first_slot;  // contributing CTAs, slot of the first
   int64_t row0, col0, g_rows;           // tile origin in C; rows of the group
   float alpha;
+  int32_t d;                            // accumulator buffer of the segment
+  uint32_t has;                         // bit t: issuer t's accumulator contributes
   int32_t valid;
 };
 
@@ -500,6 +510,22 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const float alpha = p.alpha_dev ? alpha_dev : p.group_alpha[ec.g];
       cursor_next<BN>(p, ec);
       const int d = static_cast<int>(seg % C::kNumD);
+      // split tile: its contributors and their partial slots (every
+      // contributor but the first starts inside the tile, slot 2c; the first
+      // uses its second slot unless its range starts at the tile)
+      int64_t c_first = 0, c_last = 0, first_slot = 0;
+      uint32_t* ctr = nullptr;
+      const bool last_seg = seg_end == u1;
+      bool early = false;   // every other contributor has arrived: sum now
+      if (!full_tile) {
+        c_first = cta_of_unit(tile * KS, U, P);
+        c_last = cta_of_unit((tile + 1) * KS - 1, U, P);
+        first_slot = 2 * c_first + ((c_first * U / P) / KS == tile ? 0 : 1);
+        ctr = &p.counters[c_first];
+        // first look while the segment's MMAs run
+        if (last_seg && epi_tid == 0)
+          *epi_flag = ld_acquire_gpu(ctr) == static_cast<uint32_t>(c_last - c_first);
+      }
       if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
       // issuer t wrote its accumulator iff the segment holds a unit with
@@ -510,6 +536,33 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
       for (int t = 0; t < C::kMmaThreads; ++t)
         if ((t - seg_r0 + C::kMmaThreads) % C::kMmaThreads < seg_len) has |= 1u << t;
+      if (!full_tile && last_seg) {
+        // second look once the MMAs are done
+        if (epi_tid == 0 && !*epi_flag)
+          *epi_flag = ld_acquire_gpu(ctr) == static_cast<uint32_t>(c_last - c_first);
+        if (!epi_sync()) break;
+        early = *epi_flag != 0;
+        if (early) {
+          // the CTA's last segment, summed by all warps after the final
+          // barrier from the accumulator that stays in tensor memory
+          if (epi_tid == 0) {
+            atomicExch(ctr, 0u);   // no other contributor touches it again
+            fix->c_g = c_g;
+            fix->c_first = c_first;
+            fix->c_last = c_last;
+            fix->first_slot = first_slot;
+            fix->row0 = static_cast<int64_t>(mt) * BN;
+            fix->col0 = static_cast<int64_t>(nt) * kTileN;
+            fix->g_rows = g_rows;
+            fix->alpha = alpha;
+            fix->d = d;
+            fix->has = has;
+            fix->valid = 1;
+          }
+          u = seg_end;
+          continue;
+        }
+      }
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
       const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
@@ -547,12 +600,6 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&dempty[d]));
       if (!full_tile) {
-        // stream-K fix-up: the last contributor sums all partials in CTA order
-        const int64_t c_first = cta_of_unit(tile * KS, U, P);
-        const int64_t c_last = cta_of_unit((tile + 1) * KS - 1, U, P);
-        // every contributor but the first starts inside this tile (slot 2c);
-        // the first uses its second slot unless its range starts at the tile
-        const int64_t first_slot = 2 * c_first + ((c_first * U / P) / KS == tile ? 0 : 1);
         // Ordering without per-thread fences: the group barrier (mbarrier
         // arrive = release, wait = acquire, CTA scope) orders every epilogue
         // thread's partial stores before thread 0's GPU-scope acq_rel
@@ -561,13 +608,13 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         // threads through its own group barrier before their loads.
         if (!epi_sync()) break;
         if (epi_tid == 0) {
-          const uint32_t old = atomic_add_acq_rel_gpu(&p.counters[c_first], 1u);
+          const uint32_t old = atomic_add_acq_rel_gpu(ctr, 1u);
           const int is_last = (static_cast<int64_t>(old) == c_last - c_first);
-          if (is_last) atomicExch(&p.counters[c_first], 0u);  // ready for the next call
+          if (is_last) atomicExch(ctr, 0u);  // ready for the next call
           *epi_flag = is_last;
         }
         if (!epi_sync()) break;
-        if (*epi_flag && seg_end == u1) {
+        if (*epi_flag && last_seg) {
           // the CTA's last segment: summed by all warps after the final barrier
           if (epi_tid == 0) {
             fix->c_g = c_g;
@@ -578,6 +625,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             fix->col0 = static_cast<int64_t>(nt) * kTileN;
             fix->g_rows = g_rows;
             fix->alpha = alpha;
+            fix->d = d;
+            fix->has = has;
             fix->valid = 1;
           }
         } else if (*epi_flag) {
@@ -591,7 +640,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll 1
             for (int64_t cb = c_first; cb <= c_last; cb += kFixBatch) {
-              float t[kFixBatch][16];
+              float tv[kFixBatch][16];
 #pragma unroll
               for (int x = 0; x < kFixBatch; ++x) {
                 const int64_t c = cb + x;
@@ -600,14 +649,14 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
                   const float* src =
                       p.partials + static_cast<size_t>(cs) * (BN * kTileN) + c0 * kTileN + r;
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) t[x][j] = __ldcg(src + j * kTileN);
+                  for (int j = 0; j < 16; ++j) tv[x][j] = __ldcg(src + j * kTileN);
                 }
               }
 #pragma unroll
               for (int x = 0; x < kFixBatch; ++x) {
                 if (cb + x <= c_last) {
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
+                  for (int j = 0; j < 16; ++j) acc[j] += tv[x][j];
                 }
               }
             }
@@ -700,58 +749,90 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-  // a wait that ran out anywhere in the CTA is reported by thread 0, which
-  // has passed the grid dependency wait
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
 
-  // Deferred fix-up of the last segment's tile (see FixJob), by all threads:
-  // element e = activation row * 128 + weight row, as in a partial slot, so
-  // consecutive threads read and write consecutive addresses.  Partials are
-  // added in CTA order, as in the epilogue.  The epilogue's acquire of the
-  // arrival counter reaches every thread through the barrier above.
+  // Deferred sum of the last segment's split tile (see FixJob), by the
+  // warps of kFixGroups groups of four (one warp per tensor-memory lane
+  // quarter), each group taking BN / kFixGroups activation rows: a thread
+  // owns one weight row r, reads this CTA's accumulator for its rows from
+  // tensor memory and the other contributors' partials (consecutive threads
+  // at consecutive addresses), adds them in CTA order and writes C.  The
+  // epilogue's acquire of the arrival counter reaches every thread through
+  // the barrier above.
   if (fix->valid && !*abort_flag) {
     const FixJob f = *fix;
-    constexpr int kElems = BN * kTileN;
-    constexpr int kStride = C::kThreads;
+    constexpr int kFixGroups = C::kThreads / 32 >= 16 ? 4 : 2;
+    constexpr int kCols = BN / kFixGroups;               // activation rows per group
+    constexpr int kLd = kCols >= 16 ? 16 : 4;            // columns per tensor-memory load
+    const int fg = warp >> 2;
+    if (fg < kFixGroups && !*abort_flag) {
+      const int q = warp & 3;
+      const int r = 32 * q + lane;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase +
+                             f.d * BN + fg * kCols;
 #pragma unroll 1
-    for (int e0 = threadIdx.x; e0 < kElems; e0 += 16 * kStride) {
-      float acc[16];
+      for (int c0 = 0; c0 < kCols; c0 += kLd) {
+        float own[kLd];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < kLd; ++j) own[j] = 0.0f;
+        bool have = false;
+#pragma unroll
+        for (int t = 0; t < C::kMmaThreads; ++t) {
+          if (f.has & (1u << t)) {
+            uint32_t x[kLd];
+            if constexpr (kLd == 16) {
+              tmem_ld_x16(tbase + (t * C::kNumD) * BN + c0, x);
+            } else {
+              tmem_ld_x4(tbase + (t * C::kNumD) * BN + c0, x);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < kLd; ++j) own[j] = have ? own[j] + __uint_as_float(x[j]) : __uint_as_float(x[j]);
+            have = true;
+          }
+        }
+        const int m0 = fg * kCols + c0;   // first activation row (tile-local)
+        float acc[kLd];
+#pragma unroll
+        for (int j = 0; j < kLd; ++j) acc[j] = 0.0f;
 #pragma unroll 1
-      for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
-        float t[kFixBatch][16];
+        for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
+          float tv[kFixBatch][kLd];
 #pragma unroll
-        for (int x = 0; x < kFixBatch; ++x) {
-          const int64_t c = cb + x;
-          if (c <= f.c_last) {
-            const float* src =
-                p.partials + static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * c) * kElems;
+          for (int x = 0; x < kFixBatch; ++x) {
+            const int64_t c = cb + x;
+            if (c <= f.c_last && c != cta) {
+              const float* src = p.partials +
+                                 static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * c) *
+                                     (BN * kTileN) +
+                                 m0 * kTileN + r;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int e = e0 + j * kStride;
-              t[x][j] = e < kElems ? __ldcg(src + e) : 0.0f;
+              for (int j = 0; j < kLd; ++j) tv[x][j] = __ldcg(src + j * kTileN);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < kFixBatch; ++x) {
+            const int64_t c = cb + x;
+            if (c <= f.c_last) {
+#pragma unroll
+              for (int j = 0; j < kLd; ++j) acc[j] += c == cta ? own[j] : tv[x][j];
             }
           }
         }
 #pragma unroll
-        for (int x = 0; x < kFixBatch; ++x) {
-          if (cb + x <= f.c_last) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] += t[x][j];
-          }
+        for (int j = 0; j < kLd; ++j) {
+          const int64_t mrow = f.row0 + m0 + j;
+          if (mrow < f.g_rows) f.c_g[mrow * p.n + f.col0 + r] = out_bits<FMT>(f.alpha * acc[j]);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = e0 + j * kStride;
-        const int64_t mrow = f.row0 + (e >> 7);
-        if (e < kElems && mrow < f.g_rows)
-          f.c_g[mrow * p.n + f.col0 + (e & (kTileN - 1))] = out_bits<FMT>(f.alpha * acc[j]);
-      }
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
   }
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  // a wait that ran out anywhere in the CTA is reported by thread 0, which
+  // has passed the grid dependency wait
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
 }
 
 template <int FMT, int BN, int KU>

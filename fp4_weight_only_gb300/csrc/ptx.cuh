@@ -96,6 +96,18 @@ __device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* addr, uint3
   return old;
 }
 
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Atomic add with release semantics at GPU scope, no return value.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* addr, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------------- copies
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
@@ -201,6 +213,14 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 4 columns of 32-bit words.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
