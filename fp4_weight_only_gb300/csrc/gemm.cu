@@ -23,7 +23,7 @@
 // * Warp roles:
 //     warp 0      producer: the two copies per unit into a ring of
 //                 shared-memory stages (mbarrier full/empty);
-//     warp 1      tensor-memory owner and MMA issuer (one thread);
+//     warp 1      tensor-memory owner and MMA issuer (one elected lane);
 //     warps 2-5   epilogue: tensor memory -> registers -> C or partials;
 //     warps 6-13  dequantisers: shared memory -> registers -> BF16 -> tensor
 //                 memory, where the MMA reads its A operand.  Each thread owns
@@ -137,6 +137,60 @@ __device__ __forceinline__ void cursor_next(const Params& p, TileCursor& c) {
   c.m_tiles = c.g < p.num_groups ? group_m_tiles<BN>(p, c.g) : 0;
   c.row0 = c.g < p.num_groups ? p.row_off[c.g] : 0;
 }
+
+// The weight-chunk stream of a CTA: unit by unit, the unit's KU repacked
+// chunks (contiguous codes + scales) by one bulk copy into the next weight
+// stage.  Addresses advance incrementally (a runtime 64-bit division costs
+// hundreds of cycles in a single thread): the consecutive units of a tile
+// are adjacent chunks, so the source moves on by one unit's bytes and is
+// recomputed only at a tile boundary; stage addresses move on by one stage
+// and wrap.
+template <int FMT, int BN, int KU>
+struct WeightStream {
+  static constexpr uint32_t kBytes = KU * FmtTraits<FMT>::kChunkBytes;
+  const uint8_t* src;
+  int64_t KS;            // units per tile
+  int32_t ku;            // unit index inside the tile
+  TileCursor cur;
+  uint32_t dst, dst0;    // shared-memory stage, first stage
+  uint32_t bar, full0;   // stage * 8, address of the stage-0 full barrier
+  uint32_t ph;           // phase of the stage's free barrier to wait for, ^ 1
+  int32_t stages;
+
+  __device__ __forceinline__ void init(const Params& p, int64_t u0, int64_t ks, uint32_t sm_w,
+                                       uint32_t wfull0, int32_t nstages) {
+    KS = ks;
+    const int64_t tile = u0 / KS;
+    ku = static_cast<int32_t>(u0 - tile * KS);
+    cur = cursor_at<BN>(p, tile);
+    src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, ku * KU, KS * KU);
+    dst = dst0 = sm_w;
+    bar = 0;
+    full0 = wfull0;
+    ph = 0;
+    stages = nstages;
+  }
+  __device__ __forceinline__ void advance(const Params& p) {
+    src += kBytes;
+    dst += kBytes;
+    bar += 8;
+    if (bar == 8u * stages) {
+      bar = 0;
+      dst = dst0;
+      ph ^= 1u;
+    }
+    if (++ku == KS) {
+      ku = 0;
+      cursor_next<BN>(p, cur);
+      src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, 0, KS * KU);
+    }
+  }
+  __device__ __forceinline__ void issue(const Params& p, uint64_t policy) {
+    mbar_arrive_expect_tx(full0 + bar, kBytes);
+    bulk_g2s(dst, src, kBytes, full0 + bar, policy);
+    advance(p);
+  }
+};
 
 template <int FMT, int BN, int KU>
 struct Cfg {
@@ -333,48 +387,29 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const int64_t nu = u1 - u0;
       const int64_t tile0 = u0 / KS;
       const int64_t ku0 = u0 - tile0 * KS;
-      int64_t wi = 0, xi = 0;           // next unit (CTA-local) of each stream
-      uint32_t wph = 0, xph = 0;
-      int32_t w_ku = static_cast<int32_t>(ku0), x_ku = w_ku;
-      TileCursor wc = cursor_at<BN>(p, tile0), xc = wc;
-      // running addresses: the consecutive units of a tile are adjacent
-      // chunks, so the weight source advances by one unit's bytes and is
-      // recomputed only at a tile boundary; stage addresses advance by one
-      // stage and wrap
-      const uint8_t* wsrc =
-          p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, w_ku * KU, KS * KU);
+      // the first ring of weight chunks was issued by an epilogue thread
+      // before the grid dependency wait; this stream continues after it
+      WeightStream<FMT, BN, KU> ws;
+      ws.init(p, u0, KS, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      int64_t wi = nu < C::kWStages ? nu : C::kWStages;
+      for (int64_t j = 0; j < wi; ++j) ws.advance(p);
+      int64_t xi = 0;
+      uint32_t xph = 0;
+      int32_t x_ku = static_cast<int32_t>(ku0);
+      TileCursor xc = cursor_at<BN>(p, tile0);
       int32_t xrow = xc.row0 + xc.mt * BN, xk = x_ku * 2 * KU;
-      const uint32_t wdst0 = smem_u32(sm_w), xdst0 = smem_u32(sm_a);
-      const uint32_t wfree0 = smem_u32(&wfree[0]), wfull0 = smem_u32(&wfull[0]);
+      const uint32_t xdst0 = smem_u32(sm_a);
+      const uint32_t wfree0 = smem_u32(&wfree[0]);
       const uint32_t mdone0 = smem_u32(&mdone[0]), xfull0 = smem_u32(&xfull[0]);
-      uint32_t wdst = wdst0, xdst = xdst0, wbar = 0, xbar = 0;   // bar: stage * 8
-      auto issue_weights = [&]() {
-        mbar_arrive_expect_tx(wfull0 + wbar, C::kWBytes);
-        bulk_g2s(wdst, wsrc, C::kWBytes, wfull0 + wbar, policy);
-        ++wi;
-        wsrc += C::kWBytes;
-        wdst += C::kWBytes;
-        wbar += 8;
-        if (wbar == 8 * C::kWStages) {
-          wbar = 0;
-          wdst = wdst0;
-          wph ^= 1u;
-        }
-        if (++w_ku == KS) {
-          w_ku = 0;
-          cursor_next<BN>(p, wc);
-          wsrc = p.rep + wc.g * p.rep_stride + chunk_offset<FMT>(wc.nt, 0, KS * KU);
-        }
-      };
-      // the first ring of weight chunks goes out before the grid dependency
-      // wait (every stage starts free)
-      while (wi < nu && wi < C::kWStages) issue_weights();
+      uint32_t xdst = xdst0, xbar = 0;   // bar: stage * 8
+      // activations may be written by the previous kernel on the stream
       grid_dependency_wait();
       const uint64_t t0 = global_timer_ns();
       for (uint32_t spin = 0; wi < nu || xi < nu;) {
         bool progress = false;
-        if (wi < nu && mbar_test_wait(wfree0 + wbar, wph ^ 1u)) {
-          issue_weights();
+        if (wi < nu && mbar_test_wait(wfree0 + ws.bar, ws.ph ^ 1u)) {
+          ws.issue(p, policy);
+          ++wi;
           progress = true;
         }
         if (xi < nu && mbar_test_wait(mdone0 + xbar, xph ^ 1u)) {
@@ -397,6 +432,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           }
           progress = true;
         }
+        // nothing to issue: back off briefly instead of taking issue slots
+        // from the dequantiser warps of this sub-partition
+        if (!progress) __nanosleep(128);
         if (!progress && (++spin & 63u) == 0) {
           if (*abort_flag) break;
           if (global_timer_ns() - t0 > p.timeout_ns) {
@@ -420,7 +458,14 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   } else if (warp == kMmaWarp || warp > C::kMmaWarpX) {
     // ------------------------------------------------------------ MMA issue
     const int t = warp == kMmaWarp ? 0 : warp - C::kMmaWarpX;   // issues units i % kMmaThreads == t
-    if (lane == 0) {
+    // The whole warp runs the loop, so every operand of tcgen05.mma is
+    // warp-uniform and can stay in uniform registers; one elected lane
+    // issues the MMAs and commits.  (Issued from a lone lane-0 branch each
+    // MMA cost ~65 cycles of issue, which set the pace of the MMA chain.)
+    {
+      auto uwait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait(bar, parity));
+      };
       int64_t seg = 0;
       int st = 0, b = 0;
       uint32_t ph = 0, pb = 0;
@@ -436,29 +481,33 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           // dfull arrival for this segment then cannot overtake the other
           // issuer's arrival for the segment that last used accumulator d.
           seg_started = false;
-          if (!wait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
+          if (!uwait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
         }
         if (owner == t) {
-          if (!wait(&xfull[st], ph)) break;
-          if (!wait(&afull[b], pb)) break;
+          if (!uwait(&xfull[st], ph)) break;
+          if (!uwait(&afull[b], pb)) break;
           tc_fence_after();
           const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
           const uint32_t d_tmem = tmem + C::kDColBase + (t * C::kNumD + d) * BN;
           const uint32_t a_tmem = tmem + b * C::kAColsPerUnit;
+          if (elect_one()) {
 #pragma unroll
-          for (int j = 0; j < KU * (kStageK / 16); ++j) {
-            // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
-            const uint64_t bdesc = smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) +
-                                   (((j & 3) * 32) >> 4);
-            mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
-                       (!seg_started && j == 0) ? 0u : 1u);
+            for (int j = 0; j < KU * (kStageK / 16); ++j) {
+              // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
+              const uint64_t bdesc = smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) +
+                                     (((j & 3) * 32) >> 4);
+              mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
+                         (!seg_started && j == 0) ? 0u : 1u);
+            }
+            mma_commit(smem_u32(&mdone[st]));
           }
-          mma_commit(smem_u32(&mdone[st]));
+          __syncwarp();
           seg_started = true;
         }
         if (last) {
           // every issuer arrives once per segment, when its MMAs are done
-          mma_commit(smem_u32(&dfull[d]));
+          if (elect_one()) mma_commit(smem_u32(&dfull[d]));
+          __syncwarp();
           ++seg;
         }
         if (++st == C::kXStages) {
@@ -473,7 +522,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         if (++owner == C::kMmaThreads) owner = 0;
       }
       // all issued MMAs complete before tensor memory is released
-      mma_commit(smem_u32(&fin[t]));
+      if (elect_one()) mma_commit(smem_u32(&fin[t]));
+      __syncwarp();
       mbar_wait_bounded(smem_u32(&fin[t]), 0, p.timeout_ns, nullptr);
     }
   } else if (warp < kDeqWarp0) {
@@ -483,6 +533,16 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     const int epi_tid = threadIdx.x - kEpiWarp0 * 32;
     int64_t seg = 0;
     const int64_t first_tile_of_cta = u0 / KS;
+    if (warp == kEpiWarp0 && lane == 0) {
+      // The first ring of weight chunks, before the grid dependency wait
+      // (every stage starts free).  Issuing a bulk copy takes a while, so
+      // this idle thread does it and the producer reaches the dependency
+      // wait, and the activation copies after it, without delay.
+      WeightStream<FMT, BN, KU> ws;
+      ws.init(p, u0, KS, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      const uint64_t policy = p.weights_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
+      for (int64_t j = 0; j < u1 - u0 && j < C::kWStages; ++j) ws.issue(p, policy);
+    }
     // C, the partials and the counters may be in use by the previous kernel
     // on the stream until it has completed
     grid_dependency_wait();
