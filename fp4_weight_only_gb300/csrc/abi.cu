@@ -16,6 +16,8 @@ using petit::kNVFP4F16;
 
 constexpr int64_t kMaxDim = int64_t(1) << 24;
 constexpr uint64_t kGemmTimeoutNs = 2000000000ull;  // no legitimate wait lasts 2 s
+// the kernel counts a CTA's pipeline units in 32 bits
+constexpr int64_t kMaxUnits = int64_t(1) << 31;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -113,6 +115,7 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   int sms = 0;
   if (petit_status_t st = current_device(&sms)) return st;
   const petit::GemmPlan plan = petit::plan_gemm(m, n, k, fmt, sms);
+  if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
@@ -160,6 +163,7 @@ petit_status_t moe_common(int fmt, const void* A, const uint8_t* rep, const floa
   if (petit_status_t st = current_device(&sms)) return st;
   const petit::GemmPlan plan =
       petit::plan_grouped(off, static_cast<int>(num_experts), n, k, fmt, sms);
+  if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
@@ -421,6 +425,7 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
   int sms = 0;
   if (petit_status_t st = current_device(&sms)) return st;
   const petit::GemmPlan plan = petit::plan_gemm(m, n, k, kNVFP4, sms);
+  if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (plan.ws.total > kNoAllocScratchBytes) return PETIT_ERR_WORKSPACE;  // problem too large
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PETIT_ERR_CUDA;

@@ -466,26 +466,32 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       auto uwait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, wait(bar, parity));
       };
-      int64_t seg = 0;
-      int st = 0, b = 0;
+      // Segments (the CTA's units inside one tile) in order; inside a
+      // segment only this issuer's units i = t, t + kMmaThreads, ...
+      // (CTA-local), whose activation stage, A-buffer and phases advance by
+      // kMmaThreads (a divisor of kXStages and kNumA).  32-bit counters: a
+      // CTA has fewer than 2^31 units.
+      const int32_t nu = static_cast<int32_t>(u1 - u0);
+      const int32_t ks = static_cast<int32_t>(KS);
+      const int32_t ku0 = static_cast<int32_t>(u0 - (u0 / KS) * KS);
+      int32_t seg = 0;
+      int32_t i = t;
+      int st = t, b = t;   // t < kMmaThreads <= kNumA <= kXStages
       uint32_t ph = 0, pb = 0;
-      int64_t ku = u0 - (u0 / KS) * KS;
-      bool seg_started = false;   // this issuer has written its accumulator in this segment
-      int owner = 0;   // CTA-local unit index modulo kMmaThreads
-      for (int64_t u = u0; u < u1; ++u) {
-        const bool first = (u == u0) || (ku == 0);
-        const bool last = (u == u1 - 1) || (ku == KS - 1);
-        const int d = static_cast<int>(seg % C::kNumD);
-        if (first) {
-          // Every issuer waits here, owning a unit of the segment or not: its
-          // dfull arrival for this segment then cannot overtake the other
-          // issuer's arrival for the segment that last used accumulator d.
-          seg_started = false;
-          if (!uwait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
-        }
-        if (owner == t) {
-          if (!uwait(&xfull[st], ph)) break;
-          if (!uwait(&afull[b], pb)) break;
+      bool ok = true;
+      for (int32_t s0 = 0; s0 < nu && ok;) {
+        const int32_t s1 = min(nu, s0 + (ks - (ku0 + s0) % ks));   // next tile boundary
+        const int d = seg % C::kNumD;
+        // Every issuer waits here, owning a unit of the segment or not: its
+        // dfull arrival for this segment then cannot overtake the other
+        // issuer's arrival for the segment that last used accumulator d.
+        if (!uwait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
+        bool seg_started = false;   // this issuer has written its accumulator in this segment
+        for (; i < s1; i += C::kMmaThreads) {
+          if (!uwait(&xfull[st], ph) || !uwait(&afull[b], pb)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
           const uint32_t d_tmem = tmem + C::kDColBase + (t * C::kNumD + d) * BN;
@@ -503,23 +509,23 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
           }
           __syncwarp();
           seg_started = true;
+          st += C::kMmaThreads;
+          if (st >= C::kXStages) {
+            st -= C::kXStages;
+            ph ^= 1u;
+          }
+          b += C::kMmaThreads;
+          if (b >= C::kNumA) {
+            b -= C::kNumA;
+            pb ^= 1u;
+          }
         }
-        if (last) {
-          // every issuer arrives once per segment, when its MMAs are done
-          if (elect_one()) mma_commit(smem_u32(&dfull[d]));
-          __syncwarp();
-          ++seg;
-        }
-        if (++st == C::kXStages) {
-          st = 0;
-          ph ^= 1u;
-        }
-        if (++b == C::kNumA) {
-          b = 0;
-          pb ^= 1u;
-        }
-        if (++ku == KS) ku = 0;
-        if (++owner == C::kMmaThreads) owner = 0;
+        if (!ok) break;
+        // every issuer arrives once per segment, when its MMAs are done
+        if (elect_one()) mma_commit(smem_u32(&dfull[d]));
+        __syncwarp();
+        ++seg;
+        s0 = s1;
       }
       // all issued MMAs complete before tensor memory is released
       if (elect_one()) mma_commit(smem_u32(&fin[t]));
@@ -737,71 +743,82 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     // both 64-k halves of its 32 rows, one 32-k group pair at a time.  The
     // dequantiser warps of an SM sub-partition then work on different
     // units, so one's barrier waits and round trips overlap the others'
-    // decode arithmetic.
+    // decode arithmetic.  Only shared and tensor memory are touched, so the
+    // first units are dequantised before the previous kernel has finished.
     const int grp = (warp - kDeqWarp0) / kDeqGroupWarps;
     const int q = warp & 3;         // tensor-memory lane quarter
     const int r = 32 * q + lane;    // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    int64_t i = 0;
-    int owner = 0;                // unit i's group: i % kDeqGroups
-    int st = 0, b = 0, st2 = 0;   // st: weight stage of unit i; st2: activation stage of i - kNumA
-    uint32_t ph = 0, ph2 = 0;
-    for (int64_t u = u0; u < u1; ++u, ++i) {
-      if (owner == grp) {
-        if (!wait(&wfull[st], ph)) break;
-        bool ok = true;
+    constexpr int G = C::kDeqGroups;
+    // this group's units i = grp, grp + G, ... (CTA-local); the weight
+    // stage, A-buffer and the activation stage of unit i - kNumA advance by
+    // G and wrap (G <= kNumA <= kXStages, G <= kWStages)
+    const int32_t nu = static_cast<int32_t>(u1 - u0);
+    int st = grp, b = grp;
+    uint32_t ph = 0;
+    // first own unit that reuses an A-buffer: i0 >= kNumA, i0 = grp (mod G)
+    constexpr int kFirstReuse0 = (C::kNumA + G - 1) / G * G;   // for grp = 0
+    const int i0 = kFirstReuse0 + grp - (kFirstReuse0 - G + grp >= C::kNumA ? G : 0);
+    int st2 = (i0 - C::kNumA) % C::kXStages;
+    uint32_t ph2 = ((i0 - C::kNumA) / C::kXStages) & 1;
+    for (int32_t i = grp; i < nu; i += G) {
+      if (!wait(&wfull[st], ph)) break;
+      bool ok = true;
 #pragma unroll
-        for (int hj = 0; hj < 2 * KU; ++hj) {
-          const int h = hj / KU, j = hj % KU;
-          const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
-          const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
-          const uint4 g1 = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
-          uint32_t o[2][16];
-          if constexpr (FMT == kNVFP4 || FMT == kNVFP4F16) {
-            const uint32_t sv =
-                *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
-            decode_group<FMT>(g0, sv & 0xFFFFu, o[0]);
-            decode_group<FMT>(g1, sv >> 16, o[1]);
-          } else {
-            const uint32_t sv =
-                *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
-            decode_group<FMT>(g0, sv & 0xFFu, o[0]);
-            decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
-          }
-          if (hj == 2 * KU - 1) {
-            // the decode consumed every byte this warp read: release the chunk
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
-          }
-          if (hj == 0 && i >= C::kNumA) {
-            // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
-            // and order the stores below after their operand reads
-            if (!wait(&mdone[st2], ph2)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          const uint32_t acol =
-              tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
-          tmem_st_x16(acol, o[0]);
-          tmem_st_x16(acol + 16, o[1]);
+      for (int hj = 0; hj < 2 * KU; ++hj) {
+        const int h = hj / KU, j = hj % KU;
+        const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+        const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+        const uint4 g1 = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+        uint32_t o[2][16];
+        if constexpr (FMT == kNVFP4 || FMT == kNVFP4F16) {
+          const uint32_t sv =
+              *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
+          decode_group<FMT>(g0, sv & 0xFFFFu, o[0]);
+          decode_group<FMT>(g1, sv >> 16, o[1]);
+        } else {
+          const uint32_t sv =
+              *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
+          decode_group<FMT>(g0, sv & 0xFFu, o[0]);
+          decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
         }
-        if (!ok) break;
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
+        if (hj == 2 * KU - 1) {
+          // the decode consumed every byte this warp read: release the chunk
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
+        }
+        if (hj == 0 && i >= C::kNumA) {
+          // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
+          // and order the stores below after their operand reads
+          if (!wait(&mdone[st2], ph2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t acol =
+            tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+        tmem_st_x16(acol, o[0]);
+        tmem_st_x16(acol + 16, o[1]);
       }
-      if (++owner == C::kDeqGroups) owner = 0;
-      if (++st == C::kWStages) {
-        st = 0;
+      if (!ok) break;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
+      st += G;
+      if (st >= C::kWStages) {
+        st -= C::kWStages;
         ph ^= 1u;
       }
-      if (++b == C::kNumA) b = 0;
-      if (i >= C::kNumA && ++st2 == C::kXStages) {
-        st2 = 0;
-        ph2 ^= 1u;
+      b += G;
+      if (b >= C::kNumA) b -= C::kNumA;
+      if (i >= C::kNumA) {
+        st2 += G;
+        if (st2 >= C::kXStages) {
+          st2 -= C::kXStages;
+          ph2 ^= 1u;
+        }
       }
     }
   }
