@@ -33,7 +33,9 @@
 //   the FP4 chunk and the activation tile.
 // * Every wait is bounded; a wait that runs out records a timeout in the
 //   workspace status word and the CTA shuts down cleanly.
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -64,6 +66,9 @@ struct Params {
   int32_t k_units;          // units per tile = k / (128 * KU)
   int64_t units;
   int32_t num_ctas;
+  int32_t units_q, units_r; // units / num_ctas, units % num_ctas
+  int32_t use_bounds;       // CTA c covers [bound[c], bound[c+1]) (else an even split)
+  int32_t bound[kMaxBoundCtas + 1];
   int32_t weights_reused;   // a group has several activation tiles
   uint64_t timeout_ns;
   const float* alpha_dev;   // nullable: device-resident factor, times alpha_scale
@@ -149,7 +154,7 @@ template <int FMT, int BN, int KU>
 struct WeightStream {
   static constexpr uint32_t kBytes = KU * FmtTraits<FMT>::kChunkBytes;
   const uint8_t* src;
-  int64_t KS;            // units per tile
+  int32_t KS;            // units per tile
   int32_t ku;            // unit index inside the tile
   TileCursor cur;
   uint32_t dst, dst0;    // shared-memory stage, first stage
@@ -157,11 +162,11 @@ struct WeightStream {
   uint32_t ph;           // phase of the stage's free barrier to wait for, ^ 1
   int32_t stages;
 
-  __device__ __forceinline__ void init(const Params& p, int64_t u0, int64_t ks, uint32_t sm_w,
-                                       uint32_t wfull0, int32_t nstages) {
+  // starting at unit ku of tile `tile`
+  __device__ __forceinline__ void init(const Params& p, int32_t tile, int32_t ku0, int32_t ks,
+                                       uint32_t sm_w, uint32_t wfull0, int32_t nstages) {
     KS = ks;
-    const int64_t tile = u0 / KS;
-    ku = static_cast<int32_t>(u0 - tile * KS);
+    ku = ku0;
     cur = cursor_at<BN>(p, tile);
     src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, ku * KU, KS * KU);
     dst = dst0 = sm_w;
@@ -275,10 +280,26 @@ __device__ __forceinline__ uint16_t out_bits(float x) {
   else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// CTA that owns stream-K unit u when U units are split over P CTAs with
-// CTA c covering [floor(c U / P), floor((c+1) U / P)).
-__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t P) {
-  return ((u + 1) * P + U - 1) / U - 1;
+// First unit of CTA c's stream-K range (c = P: the end of the last).  An
+// even split is floor(c U / P) = c q + c r / P with q = U / P, r = U % P;
+// c r < P^2 fits 32 bits, so no 64-bit division is needed (this sits before
+// the producer's first activation copy, on the critical path of the CTAs
+// that start last).
+__device__ __forceinline__ int32_t cta_lo(const Params& p, int32_t c) {
+  return p.use_bounds ? p.bound[c] : c * p.units_q + (c * p.units_r) / p.num_ctas;
+}
+
+// CTA whose stream-K range holds unit u.
+__device__ __forceinline__ int32_t cta_of_unit(const Params& p, int64_t u) {
+  if (!p.use_bounds)
+    return static_cast<int32_t>(((u + 1) * p.num_ctas + p.units - 1) / p.units - 1);
+  int lo = 0, hi = p.num_ctas - 1;   // the last c with bound[c] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.bound[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 template <int FMT, int BN, int KU>
@@ -319,9 +340,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   const int64_t U = p.units;
   const int64_t P = p.num_ctas;
   const int64_t cta = blockIdx.x;
-  const int64_t u0 = cta * U / P;
-  const int64_t u1 = (cta + 1) * U / P;
+  const int64_t u0 = cta_lo(p, blockIdx.x);
+  const int64_t u1 = cta_lo(p, blockIdx.x + 1);
   const int64_t KS = p.k_units;
+  const int32_t ks32 = p.k_units;
+  const int32_t tile0_32 = static_cast<int32_t>(u0) / ks32;         // u0 < 2^31
+  const int32_t ku0_32 = static_cast<int32_t>(u0) - tile0_32 * ks32;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kWStages; ++i) {
@@ -384,18 +408,19 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       // has a free stage is issued next, weights first.  All per-unit
       // indices advance incrementally: a runtime 64-bit division costs
       // hundreds of cycles in a single thread.
-      const int64_t nu = u1 - u0;
-      const int64_t tile0 = u0 / KS;
-      const int64_t ku0 = u0 - tile0 * KS;
+      const int32_t nu = static_cast<int32_t>(u1 - u0);   // fewer than 2^31 units
+      const int32_t ks = ks32;
+      const int32_t tile0 = tile0_32;
+      const int32_t ku0 = ku0_32;
       // the first ring of weight chunks was issued by an epilogue thread
       // before the grid dependency wait; this stream continues after it
       WeightStream<FMT, BN, KU> ws;
-      ws.init(p, u0, KS, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
-      int64_t wi = nu < C::kWStages ? nu : C::kWStages;
-      for (int64_t j = 0; j < wi; ++j) ws.advance(p);
-      int64_t xi = 0;
+      ws.init(p, tile0, ku0, ks, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      int32_t wi = nu < C::kWStages ? nu : C::kWStages;
+      for (int32_t j = 0; j < wi; ++j) ws.advance(p);
+      int32_t xi = 0;
       uint32_t xph = 0;
-      int32_t x_ku = static_cast<int32_t>(ku0);
+      int32_t x_ku = ku0;
       TileCursor xc = cursor_at<BN>(p, tile0);
       int32_t xrow = xc.row0 + xc.mt * BN, xk = x_ku * 2 * KU;
       const uint32_t xdst0 = smem_u32(sm_a);
@@ -424,7 +449,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             xdst = xdst0;
             xph ^= 1u;
           }
-          if (++x_ku == KS) {
+          if (++x_ku == ks) {
             x_ku = 0;
             xk = 0;
             cursor_next<BN>(p, xc);
@@ -445,12 +470,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
-        const int64_t wfirst = wi > C::kWStages ? wi - C::kWStages : 0;
-        for (int64_t j = wfirst; j < wi; ++j)
+        const int32_t wfirst = wi > C::kWStages ? wi - C::kWStages : 0;
+        for (int32_t j = wfirst; j < wi; ++j)
           mbar_wait_bounded(smem_u32(&wfull[j % C::kWStages]), (j / C::kWStages) & 1,
                             p.timeout_ns, nullptr);
-        const int64_t xfirst = xi > C::kXStages ? xi - C::kXStages : 0;
-        for (int64_t j = xfirst; j < xi; ++j)
+        const int32_t xfirst = xi > C::kXStages ? xi - C::kXStages : 0;
+        for (int32_t j = xfirst; j < xi; ++j)
           mbar_wait_bounded(smem_u32(&xfull[j % C::kXStages]), (j / C::kXStages) & 1,
                             p.timeout_ns, nullptr);
       }
@@ -545,9 +570,24 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       // this idle thread does it and the producer reaches the dependency
       // wait, and the activation copies after it, without delay.
       WeightStream<FMT, BN, KU> ws;
-      ws.init(p, u0, KS, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      ws.init(p, tile0_32, ku0_32, ks32, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
       const uint64_t policy = p.weights_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
       for (int64_t j = 0; j < u1 - u0 && j < C::kWStages; ++j) ws.issue(p, policy);
+      // The CTAs with the highest indices take their SMs last (as the
+      // previous kernel's CTAs leave them); a CTA of the lower half pulls the
+      // first ring of weight chunks of its partner in the upper half into
+      // L2, so that partner's first copies hit L2.
+      const int32_t half = (p.num_ctas + 1) / 2;
+      if (blockIdx.x + half < p.num_ctas) {
+        const int32_t pc = blockIdx.x + half;
+        const int32_t pu0 = cta_lo(p, pc), pn = cta_lo(p, pc + 1) - pu0;
+        WeightStream<FMT, BN, KU> pw;
+        pw.init(p, pu0 / ks32, pu0 % ks32, ks32, 0, 0, C::kWStages);
+        for (int32_t j = 0; j < pn && j < C::kWStages; ++j) {
+          bulk_prefetch_l2(pw.src, WeightStream<FMT, BN, KU>::kBytes);
+          pw.advance(p);
+        }
+      }
     }
     // C, the partials and the counters may be in use by the previous kernel
     // on the stream until it has completed
@@ -584,9 +624,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const bool last_seg = seg_end == u1;
       bool early = false;   // every other contributor has arrived: sum now
       if (!full_tile) {
-        c_first = cta_of_unit(tile * KS, U, P);
-        c_last = cta_of_unit((tile + 1) * KS - 1, U, P);
-        first_slot = 2 * c_first + ((c_first * U / P) / KS == tile ? 0 : 1);
+        c_first = cta_of_unit(p, tile * KS);
+        c_last = cta_of_unit(p, (tile + 1) * KS - 1);
+        first_slot = 2 * c_first + (cta_lo(p, static_cast<int32_t>(c_first)) / KS == tile ? 0 : 1);
         ctr = &p.counters[c_first];
         // first look while the segment's MMAs run
         if (last_seg && epi_tid == 0)
@@ -960,7 +1000,54 @@ cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tma
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Stream-K ranges.  The CTAs of a launch take their SMs in index order as
+// the previous kernel's CTAs leave them, so under back-to-back launches the
+// last few indices start last -- measured on GB300 for the decode step, the
+// last four CTAs finish their MMAs ~1.5-2.5 us after the median one and the
+// lateness halves about every seven indices below them.  With equal ranges
+// they set the end of every kernel, so their ranges shrink:
+//   deficit(c) = kLateStartNs * exp((c - (P - 1)) / (P / 15)) / unit time
+// units for CTA c, and every CTA shares the total back.
+constexpr double kLateStartNs = 1600.0;
+
+void plan_bounds(GemmPlan& pl, double late_ns) {
+  const int P = pl.num_ctas;
+  const int64_t U = pl.units;
+  pl.use_bounds = false;
+  // measured on GB300: 1 % off the m = 16 decode step; with 128/256-row
+  // tiles (prefill) the skew was 1 % slower, so those keep the even split
+  if (P < 16 || P > kMaxBoundCtas || late_ns <= 0.0 || pl.bn > 64) return;
+  // rough time of one unit on one SM at the decode pace (its weight bytes
+  // at the SM's share of HBM bandwidth)
+  const double unit_ns = 240.0 * pl.ku;
+  const double tau = P / 15.0;
+  double deficit[kMaxBoundCtas], total = 0.0;
+  for (int c = 0; c < P; ++c) {
+    deficit[c] = late_ns / unit_ns * std::exp((c - (P - 1)) / tau);
+    total += deficit[c];
+  }
+  const double base = (static_cast<double>(U) + total) / P;
+  double share[kMaxBoundCtas], sum = 0.0;
+  for (int c = 0; c < P; ++c) {
+    share[c] = std::max(base - deficit[c], std::max(1.0, 0.5 * base));
+    sum += share[c];
+  }
+  double cum = 0.0;
+  pl.bound[0] = 0;
+  for (int c = 1; c < P; ++c) {
+    cum += share[c - 1] * static_cast<double>(U) / sum;
+    int64_t b = std::llround(cum);
+    b = std::max<int64_t>(b, pl.bound[c - 1] + 1);   // every CTA keeps a unit
+    b = std::min<int64_t>(b, U - (P - c));
+    pl.bound[c] = static_cast<int32_t>(b);
+  }
+  pl.bound[P] = static_cast<int32_t>(U);
+  pl.use_bounds = true;
+}
+
 std::atomic<int> g_tile_override{0};   // bn | ku << 16, or 0: the planner decides
+
+double late_start_ns() { return kLateStartNs; }
 
 }  // namespace
 
@@ -1036,6 +1123,7 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
   pl.num_ctas = static_cast<int>(pl.units < num_sms ? pl.units : num_sms);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
   if (pl.num_ctas > kMaxCtas) pl.num_ctas = kMaxCtas;
+  if (pl.units < (int64_t(1) << 31)) plan_bounds(pl, late_start_ns());
   pl.ws.counters_off = kWsHeaderBytes;
   pl.ws.partials_off = align_up(kWsHeaderBytes + kWsCountersBytes, 256);
   pl.ws.total = pl.ws.partials_off +
@@ -1061,6 +1149,11 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   prm.k_units = pl.k_stages / pl.ku;
   prm.units = pl.units;
   prm.num_ctas = pl.num_ctas;
+  prm.units_q = static_cast<int32_t>(pl.units / pl.num_ctas);
+  prm.units_r = static_cast<int32_t>(pl.units % pl.num_ctas);
+  prm.use_bounds = pl.use_bounds ? 1 : 0;
+  if (pl.use_bounds)
+    for (int c = 0; c <= pl.num_ctas; ++c) prm.bound[c] = pl.bound[c];
   prm.weights_reused = pl.weights_reused ? 1 : 0;
   prm.alpha_dev = a.alpha_dev;
   prm.alpha_scale = a.alpha_scale;

@@ -18,6 +18,9 @@ constexpr uint32_t kStatusTimeout = 1u;  // bit in the workspace status word
 // size for every problem, so no call's partials ever land on another
 // call's counters and a workspace can be shared by problems of any shape.
 constexpr size_t kWsHeaderBytes = 256;
+// Largest grid whose stream-K ranges are given as an explicit table (a
+// GB300 has 152 SMs); larger grids split the units evenly.
+constexpr int kMaxBoundCtas = 160;
 constexpr int kMaxCtas = 1024;
 constexpr size_t kWsCountersBytes = sizeof(uint32_t) * kMaxCtas;
 
@@ -41,6 +44,10 @@ struct GemmPlan {
   int k_stages;    // 128-k chunks per tile row
   int64_t units;   // tiles * k_stages / ku
   int num_ctas;
+  // stream-K ranges: CTA c covers units [bound[c], bound[c+1]) when
+  // use_bounds, else an even split
+  bool use_bounds;
+  int32_t bound[kMaxBoundCtas + 1];
   bool weights_reused;   // some group has several activation tiles
   int num_groups;
   int32_t row_off[kMaxGroups + 1];
