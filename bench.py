@@ -440,45 +440,82 @@ def run_ours(args, rank, world, local):
                 "avg_launch_us": round(avg_launch_s * 1e6, 3),
                 "peak_source": peaks["source"] + " hbm_gbs (copy bandwidth)"}
 
-    # e2e: public API per step with pinned host activations in and results out
-    # the step's four activation matrices in one pinned host buffer and its
-    # four results in another (per-layer views), so each step makes one
-    # host-to-device and one device-to-host copy
+    # e2e: the public binding in a serving loop.  Every step copies its four
+    # activation matrices in (one pinned host-to-device copy), runs the four
+    # GEMMs and copies their results out (one device-to-host copy into pinned
+    # memory), and the host reads each step's results.  Two buffer sets
+    # alternate, so step s+1's input copy (copy-in stream) and step s-1's
+    # result copy (copy-out stream) overlap step s's GEMMs, and the host
+    # waits for step s-1's results while step s runs.
     a_sizes = [M_DECODE * k for _, _, k in SHAPES]
     c_sizes = [M_DECODE * n for _, n, _ in SHAPES]
     a_host_all = torch.cat([a.reshape(-1).cpu() for a in acts]).pin_memory()
-    c_host_all = torch.empty(sum(c_sizes), dtype=torch.bfloat16).pin_memory()
-    a_dev_all = torch.empty(sum(a_sizes), dtype=torch.bfloat16, device=dev)
-    c_dev_all = torch.empty(sum(c_sizes), dtype=torch.bfloat16, device=dev)
-    a_dev = [v.view(M_DECODE, k) for v, (_, _, k) in zip(a_dev_all.split(a_sizes), SHAPES)]
-    c_dev = [v.view(M_DECODE, n) for v, (_, n, _) in zip(c_dev_all.split(c_sizes), SHAPES)]
+    c_host = [torch.empty(sum(c_sizes), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    a_dev_all = [torch.empty(sum(a_sizes), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    c_dev_all = [torch.empty(sum(c_sizes), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    a_dev = [[v.view(M_DECODE, k) for v, (_, _, k) in zip(a_dev_all[b].split(a_sizes), SHAPES)]
+             for b in range(2)]
+    c_dev = [[v.view(M_DECODE, n) for v, (_, n, _) in zip(c_dev_all[b].split(c_sizes), SHAPES)]
+             for b in range(2)]
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for b in range(2):   # every event starts recorded (buffers free)
+        for e in (in_done[b], comp_done[b], out_done[b]):
+            e.record(stream)
     e2e_steps = max(1, min(args.steps, 200))
+    checksum = [0.0]
 
     def e2e_step(s):
-        # as a serving loop would: activations in, each layer's output buffer
-        # reused, results read back and the host waits for them every step
-        a_dev_all.copy_(a_host_all, non_blocking=True)
+        b = s & 1
+        with torch.cuda.stream(cin):      # input copy once step s-2 has read buffer b
+            cin.wait_event(comp_done[b])
+            a_dev_all[b].copy_(a_host_all, non_blocking=True)
+            in_done[b].record(cin)
+        stream.wait_event(in_done[b])     # GEMMs once the input landed and step s-2's
+        stream.wait_event(out_done[b])    # results left buffer b
         for i, (name, n, k) in enumerate(SHAPES):
-            fw = sets[0][i]
-            rep = fw.rep if (s & 1) == 0 else sets[1][i]
-            binding.gemm(a_dev[i], rep, n, "nvfp4", 1.0, workspace=ws, out=c_dev[i])
-        c_host_all.copy_(c_dev_all, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+            rep = sets[0][i].rep if b == 0 else sets[1][i]
+            binding.gemm(a_dev[b][i], rep, n, "nvfp4", 1.0, workspace=ws, out=c_dev[b][i])
+        comp_done[b].record(stream)
+        with torch.cuda.stream(cout):
+            cout.wait_event(comp_done[b])
+            c_host[b].copy_(c_dev_all[b], non_blocking=True)
+            out_done[b].record(cout)
+        if s > 0:                         # the host reads step s-1's results
+            out_done[b ^ 1].synchronize()
+            checksum[0] += float(c_host[b ^ 1][0])
 
-    for s in range(3):
+    for s in range(4):
         e2e_step(s)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(e2e_steps):
         e2e_step(s)
+    out_done[(e2e_steps - 1) & 1].synchronize()
     e2e_t = time.perf_counter() - t0
+    torch.cuda.synchronize()
     h2d = sum(2 * M_DECODE * k for _, _, k in SHAPES)
     d2h = sum(2 * M_DECODE * n for _, n, _ in SHAPES)
     e2e = {"value": round(world * step_bytes * e2e_steps / e2e_t / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "path": "binding.gemm (ctypes -> C ABI) per layer, eager; one pinned host-to-device "
-                   "copy of the step's activations and one device-to-host copy of its results; "
-                   "preallocated device outputs; host synchronised every step"}
+           "ms_per_step": round(1e3 * e2e_t / e2e_steps, 5),
+           "path": "binding.gemm (ctypes -> C ABI) per layer; per step one pinned host-to-device "
+                   "copy of the step's activations and one device-to-host copy of its results, "
+                   "double-buffered on copy streams; the host reads every step's results one step "
+                   "later; host wall clock over the steps"}
+
+    # host cost of one GEMM call (enqueue only): the public binding call, timed
+    # on the host over calls that do not fill the launch queue
+    torch.cuda.synchronize()
+    host_us = []
+    for rnd in range(5):
+        t_a = time.perf_counter()
+        for r_ in range(32):
+            binding.gemm(acts[1], sets[0][1].rep, SHAPES[1][1], "nvfp4", 1.0, workspace=ws, out=outs[1])
+        host_us.append((time.perf_counter() - t_a) / 32 * 1e6)
+        torch.cuda.synchronize()
+    e2e["host_us_per_gemm_call"] = round(statistics.median(host_us), 2)
 
     # prefill m = 256 and the other per-shape lines: per-GEMM timing, each
     # shape rotating through R weight copies

@@ -1,6 +1,7 @@
 // C ABI: argument validation, problem planning, tensor-map encoding and
 // kernel dispatch.  Validation always comes first and never touches the GPU,
 // so a rejected call enqueues nothing.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -21,39 +22,48 @@ constexpr int64_t kMaxUnits = int64_t(1) << 31;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Per-device facts, probed once.  state: 0 not probed, 1 usable (CC 10.3),
+// 2 another architecture; num_sms is written before state is published
+// (release), so the common path is one acquire load and no lock.
 struct DevInfo {
-  bool probed = false;
-  bool arch_ok = false;
+  std::atomic<int> state{0};
   int num_sms = 0;
 };
 
-std::mutex g_mu;
-DevInfo g_dev[64];
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;   // only for the first probe of a device
+DevInfo g_dev[kMaxDevices];
 
-// Current device, its SM count, and whether it is a compute-capability 10.3
-// part (the only code this library contains is sm_103a).
-petit_status_t current_device(int* sms) {
+// Current device (one cudaGetDevice), its SM count, and whether it is a
+// compute-capability 10.3 part (the only code this library contains is
+// sm_103a).
+petit_status_t current_device(int* sms, int* dev_out = nullptr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return PETIT_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
   DevInfo& d = g_dev[dev];
-  if (!d.probed) {
-    int major = 0, minor = 0, n = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      return PETIT_ERR_CUDA;
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    st = d.state.load(std::memory_order_acquire);
+    if (st == 0) {
+      int major = 0, minor = 0, n = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PETIT_ERR_CUDA;
+      }
+      d.num_sms = n;
+      st = (major == 10 && minor == 3) ? 1 : 2;
+      d.state.store(st, std::memory_order_release);
     }
-    d.arch_ok = (major == 10 && minor == 3);
-    d.num_sms = n;
-    d.probed = true;
   }
   if (sms) *sms = d.num_sms;
-  return d.arch_ok ? PETIT_OK : PETIT_ERR_ARCH;
+  if (dev_out) *dev_out = dev;
+  return st == 1 ? PETIT_OK : PETIT_ERR_ARCH;
 }
 
 petit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? PETIT_OK : PETIT_ERR_CUDA; }
@@ -96,6 +106,46 @@ petit_status_t encode_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t 
   return r == CUDA_SUCCESS ? PETIT_OK : PETIT_ERR_CUDA;
 }
 
+// Activation tensor maps of recent calls, per host thread (no locking):
+// serving loops call the GEMM with the same activation buffers and shapes
+// over and over, and encoding a map costs more than the rest of the call.
+// The key is everything the map encodes.
+struct MapKey {
+  const void* A;
+  int64_t m, k;
+  int bn, ku, f16, dev;
+};
+
+petit_status_t cached_a_map(CUtensorMap* map, const void* A, int64_t m, int64_t k, int bn, int ku,
+                            bool f16, int dev) {
+  constexpr int kSlots = 8;
+  thread_local MapKey keys[kSlots];
+  thread_local CUtensorMap maps[kSlots];
+  thread_local int used = 0, next = 0;
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.A = A;
+  key.m = m;
+  key.k = k;
+  key.bn = bn;
+  key.ku = ku;
+  key.f16 = f16 ? 1 : 0;
+  key.dev = dev;
+  for (int i = 0; i < used; ++i) {
+    if (std::memcmp(&keys[i], &key, sizeof(key)) == 0) {
+      *map = maps[i];
+      return PETIT_OK;
+    }
+  }
+  std::memset(map, 0, sizeof(*map));
+  if (petit_status_t st = encode_a_map(map, A, m, k, bn, ku, f16)) return st;
+  keys[next] = key;
+  maps[next] = *map;
+  next = (next + 1) % kSlots;
+  if (used < kSlots) ++used;
+  return PETIT_OK;
+}
+
 petit_status_t check_tiled_shape(int64_t n, int64_t k) {
   if (n < petit::kTileN || k < petit::kStageK || n % petit::kTileN || k % petit::kStageK ||
       n > kMaxDim || k > kMaxDim)
@@ -112,16 +162,16 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   if (!aligned16(A) || !aligned16(rep) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
   if (!ws) return PETIT_ERR_WORKSPACE;
   if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
-  int sms = 0;
-  if (petit_status_t st = current_device(&sms)) return st;
+  int sms = 0, dev = 0;
+  if (petit_status_t st = current_device(&sms, &dev)) return st;
   const petit::GemmPlan plan = petit::plan_gemm(m, n, k, fmt, sms);
   if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku, fmt == kNVFP4F16))
+  if (petit_status_t st = cached_a_map(&map, A, m, k, plan.bn, plan.ku, fmt == kNVFP4F16, dev))
     return st;
   petit::GemmArgs args{A, rep, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  args.device = dev;
   if (alpha_dev) {
     args.alpha_dev = alpha_dev;
     args.alpha_scale = alpha;
@@ -159,16 +209,16 @@ petit_status_t moe_common(int fmt, const void* A, const uint8_t* rep, const floa
   const int64_t rows = off[num_experts];
   if (!ws) return PETIT_ERR_WORKSPACE;
   if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
-  int sms = 0;
-  if (petit_status_t st = current_device(&sms)) return st;
+  int sms = 0, dev = 0;
+  if (petit_status_t st = current_device(&sms, &dev)) return st;
   const petit::GemmPlan plan =
       petit::plan_grouped(off, static_cast<int>(num_experts), n, k, fmt, sms);
   if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, rows, k, plan.bn, plan.ku)) return st;
+  if (petit_status_t st = cached_a_map(&map, A, rows, k, plan.bn, plan.ku, false, dev)) return st;
   petit::GemmArgs args{A, rep, C, rows, n, k, alphas[0], static_cast<uint8_t*>(ws), kGemmTimeoutNs};
+  args.device = dev;
   args.rep_stride = static_cast<int64_t>(petit_repacked_bytes(n, k, fmt));
   args.group_alpha = alphas;
   return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
@@ -198,7 +248,8 @@ size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt) {
   if (n < 0 || k < 0) return 0;
   const size_t nk = static_cast<size_t>(n) * static_cast<size_t>(k);
   if (fmt == PETIT_FMT_NVFP4 || fmt == PETIT_FMT_NVFP4_F16) return nk / 2 + nk / 16;
-  if (fmt == PETIT_FMT_MXFP4) return nk / 2 + nk / 32;
+  // MXFP4 chunks (128 x 128) carry a 16-byte flag field: nk / 1024 bytes
+  if (fmt == PETIT_FMT_MXFP4) return nk / 2 + nk / 32 + nk / 1024;
   return 0;
 }
 
@@ -457,5 +508,6 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
   if (cudaMemsetAsync(scratch, 0, plan.ws.partials_off, s) != cudaSuccess) return PETIT_ERR_CUDA;
   petit::GemmArgs args{A, rep, C, m, n, k, global_scale * 256.0f, static_cast<uint8_t*>(scratch),
                        kGemmTimeoutNs};
+  args.device = dev;
   return from_cuda(petit::launch_gemm(plan, args, map, s));
 }

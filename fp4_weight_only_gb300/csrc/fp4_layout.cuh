@@ -10,8 +10,10 @@
 // which becomes the BF16 subnormal 2^-127.  One BF16x2 multiply by the block
 // scale (pre-multiplied by 2^118, exact for every E4M3 value) then yields
 // value * scale * 2^-8, exactly representable; the GEMM epilogue multiplies
-// the FP32 sum by g * 2^8.  MXFP4 uses two exact multiplies (by 2^126, then by
-// the E8M0 scale) because E8M0 covers 2^-127..2^127.
+// the FP32 sum by g * 2^8.  MXFP4 uses one exact multiply by 2^(c-1) when
+// every E8M0 code c of a chunk is at most 128 (recorded by the repack in the
+// chunk), and otherwise two (by 2^126, then by 2^(c-127)), because E8M0
+// covers 2^-127..2^127 and BF16 only up to 2^127.
 #pragma once
 
 #include <cstdint>
@@ -20,7 +22,7 @@
 
 namespace petit {
 
-constexpr int kLayoutVersion = 3;
+constexpr int kLayoutVersion = 4;
 constexpr int kTileN = 128;   // weight rows per tile (the MMA M side)
 constexpr int kStageK = 128;  // k elements per repacked chunk / pipeline stage
 constexpr int kWChunkBytes = kTileN * kStageK / 2;  // 8192
@@ -46,7 +48,11 @@ struct FmtTraits<kMXFP4> {
   static constexpr int kBlock = 32;
   static constexpr int kSChunkBytes = kTileN * kStageK / 32; // 512
   static constexpr int kScaleBytesPerHalf = 2;               // 64 k / 32
-  static constexpr int kChunkBytes = kWChunkBytes + kSChunkBytes;  // 8704
+  // after the scales: byte 0 = 1 when every E8M0 code of the chunk is at
+  // most 128 (scale <= 2), so the decode may use one multiply (see
+  // decode_group); bytes 1..15 zero
+  static constexpr int kFlagBytes = 16;
+  static constexpr int kChunkBytes = kWChunkBytes + kSChunkBytes + kFlagBytes;  // 8720
 };
 
 // ---------------------------------------------------------------- layout
@@ -61,7 +67,7 @@ struct FmtTraits<kMXFP4> {
 // Word w of a group holds k = 8w .. 8w+7 in the bit order of pack_word().
 // Scales (at byte 8192 of the chunk): half h (k = 64h .. 64h+63) of row r
 // sits at (h * 128 + r) * kScaleBytesPerHalf, byte j holding block j of that
-// half.
+// half.  MXFP4 chunks end with a 16-byte flag field (FmtTraits<kMXFP4>).
 template <int FMT>
 __host__ __device__ constexpr size_t chunk_offset(int64_t tile, int64_t stage, int64_t stages) {
   return static_cast<size_t>((tile * stages + stage) * FmtTraits<FMT>::kChunkBytes);
@@ -167,6 +173,12 @@ __device__ __forceinline__ void nv_scale_splats(uint32_t v, uint32_t& s0, uint32
   s1 = bf16x2_splat_f32(f1 * 0x1p118f);
 }
 
+// E8M0 byte c <= 128 -> BF16x2 splat of 2^(c-1): BF16 exponent field c + 126,
+// one multiply-add (FMA pipe).  value(code) * 2^-126 * 2^(c-1) = Wq exactly
+// (a power-of-two scaling; the smallest product, 2^-128, is a BF16
+// subnormal with room to spare).
+__device__ __forceinline__ uint32_t mx_fast_splat(uint32_t c) { return c * 0x00800080u + 0x3F003F00u; }
+
 // E8M0 byte -> BF16x2 splat of 2^(c-127) (c = 0 is the BF16 subnormal 2^-127).
 __device__ __forceinline__ uint32_t mx_scale_splat(uint32_t c) {
   uint32_t b = (c & 0xFFu) << 7;
@@ -180,8 +192,9 @@ constexpr uint32_t kBf16x2_2p8 = 0x43804380u;    // 2^8 in both halves
 // Decode one 16-byte group (32 codes) into 16 BF16x2 words: out[j] holds k =
 // 2j (low half) and 2j+1 (high half).  NVFP4: sc holds the two E4M3 bytes of
 // the group (k 0-15, 16-31); result = Wq * 2^-8.  MXFP4: sc holds the E8M0
-// byte; result = Wq.  NVFP4F16: FP16x2 words, result = Wq * 2^-7.
-template <int FMT>
+// byte; result = Wq (kMxFast: sc <= 128, one multiply per word instead of
+// two).  NVFP4F16: FP16x2 words, result = Wq * 2^-7.
+template <int FMT, bool kMxFast = false>
 __device__ __forceinline__ void decode_group(const uint4& g, uint32_t sc, uint32_t (&out)[16]) {
   const uint32_t w[4] = {g.x, g.y, g.z, g.w};
   if constexpr (FMT == kNVFP4F16) {
@@ -205,6 +218,15 @@ __device__ __forceinline__ void decode_group(const uint4& g, uint32_t sc, uint32
       uint32_t p[4];
       decode_word_raw(w[i], p);
       const uint32_t s = i < 2 ? s0 : s1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) out[4 * i + j] = bmul2(p[j], s);
+    }
+  } else if constexpr (kMxFast) {
+    const uint32_t s = mx_fast_splat(sc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t p[4];
+      decode_word_raw(w[i], p);
 #pragma unroll
       for (int j = 0; j < 4; ++j) out[4 * i + j] = bmul2(p[j], s);
     }

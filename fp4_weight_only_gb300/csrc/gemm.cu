@@ -819,8 +819,15 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         } else {
           const uint32_t sv =
               *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
-          decode_group<FMT>(g0, sv & 0xFFu, o[0]);
-          decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
+          // the repack's per-chunk flag (warp-uniform): one multiply per
+          // word when every scale code of the chunk is <= 128
+          if (chunk[kWChunkBytes + T::kSChunkBytes]) {
+            decode_group<FMT, true>(g0, sv & 0xFFu, o[0]);
+            decode_group<FMT, true>(g1, sv >> 8, o[1]);
+          } else {
+            decode_group<FMT>(g0, sv & 0xFFu, o[0]);
+            decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
+          }
         }
         if (hj == 2 * KU - 1) {
           // the decode consumed every byte this warp read: release the chunk
@@ -953,17 +960,17 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 }
 
 template <int FMT, int BN, int KU>
-cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t stream) {
+cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t stream, int dev) {
   using C = Cfg<FMT, BN, KU>;
-  static int attr_done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, KU>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // the dynamic shared-memory limit is raised once per device
+  static std::atomic<bool> attr_done[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, KU>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_ctas));
@@ -979,21 +986,22 @@ cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t st
 }
 
 template <int FMT>
-cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tmap, cudaStream_t s) {
+cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tmap, cudaStream_t s,
+                       int dev) {
   if (ku == 2) {
     switch (bn) {
-      case 16: return launch_t<FMT, 16, 2>(prm, tmap, s);
-      case 32: return launch_t<FMT, 32, 2>(prm, tmap, s);
-      case 64: return launch_t<FMT, 64, 2>(prm, tmap, s);
+      case 16: return launch_t<FMT, 16, 2>(prm, tmap, s, dev);
+      case 32: return launch_t<FMT, 32, 2>(prm, tmap, s, dev);
+      case 64: return launch_t<FMT, 64, 2>(prm, tmap, s, dev);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (bn) {
-    case 16: return launch_t<FMT, 16, 1>(prm, tmap, s);
-    case 32: return launch_t<FMT, 32, 1>(prm, tmap, s);
-    case 64: return launch_t<FMT, 64, 1>(prm, tmap, s);
-    case 128: return launch_t<FMT, 128, 1>(prm, tmap, s);
-    case 256: return launch_t<FMT, 256, 1>(prm, tmap, s);
+    case 16: return launch_t<FMT, 16, 1>(prm, tmap, s, dev);
+    case 32: return launch_t<FMT, 32, 1>(prm, tmap, s, dev);
+    case 64: return launch_t<FMT, 64, 1>(prm, tmap, s, dev);
+    case 128: return launch_t<FMT, 128, 1>(prm, tmap, s, dev);
+    case 256: return launch_t<FMT, 256, 1>(prm, tmap, s, dev);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1166,9 +1174,9 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   }
   for (int g = 0; g < pl.num_groups; ++g)
     prm.group_alpha[g] = a.group_alpha ? a.group_alpha[g] : a.alpha;
-  if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream);
-  if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream);
-  return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream);
+  if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);
+  if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream, a.device);
+  return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);
 }
 
 }  // namespace petit

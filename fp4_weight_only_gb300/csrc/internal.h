@@ -81,6 +81,7 @@ struct GemmArgs {
   // group's epilogue factor (host array of num_groups; null: alpha for all)
   int64_t rep_stride = 0;
   const float* group_alpha = nullptr;
+  int device = 0;   // the current device (the caller has looked it up)
 };
 
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmArgs& args, const CUtensorMap& tmap_a,

@@ -200,6 +200,19 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
       *reinterpret_cast<uint16_t*>(sdst + i * 2) = *reinterpret_cast<const uint16_t*>(src);
     }
   }
+  if constexpr (FMT == kMXFP4) {
+    // the chunk's flag: every E8M0 code <= 128, so the decode may multiply
+    // once by 2^(c - 1) (a BF16 number for those codes)
+    bool small = true;
+    for (int i = threadIdx.x; i < 2 * kTileN; i += kThreads) {
+      const int h = i >> 7, r = i & 127;
+      const uint8_t* src = sp + (t * kTileN + r) * srow_bytes + s * (2 * B) + h * B;
+      small = small && src[0] <= 128 && src[1] <= 128;
+    }
+    small = __syncthreads_and(small) != 0;
+    if (threadIdx.x == 0)
+      *reinterpret_cast<uint4*>(sdst + T::kSChunkBytes) = make_uint4(small ? 1u : 0u, 0u, 0u, 0u);
+  }
   // The GEMM reads its weights before its grid dependency wait, so it may
   // start (right after this kernel's CTAs exit) without the usual end-of-
   // kernel flush: make this thread's writes visible device-wide before it
@@ -232,7 +245,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ rep, uint16_t* __rest
       sc = cbase[kWChunkBytes + (h * 128 + r) * 2 + (g & 1)];
     }
     uint32_t o[16];
-    decode_group<FMT>(grp, sc, o);
+    if constexpr (FMT == kMXFP4) {
+      // the GEMM's two decodes, chosen by the chunk's flag
+      if (cbase[kWChunkBytes + T::kSChunkBytes]) decode_group<FMT, true>(grp, sc, o);
+      else decode_group<FMT>(grp, sc, o);
+    } else {
+      decode_group<FMT>(grp, sc, o);
+    }
     if constexpr (FMT == kNVFP4) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) o[j] = bmul2(o[j], kBf16x2_2p8);  // undo 2^-8, exact

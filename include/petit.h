@@ -87,7 +87,8 @@ const char* petit_status_string(petit_status_t status);
 /* ------------------------------------------------------------------ sizes */
 
 /* Bytes of a repacked weight buffer: n*k/2 code bytes plus n*k/16 (NVFP4) or
- * n*k/32 (MXFP4) scale bytes; 0 for an unknown format. */
+ * n*k/32 + n*k/1024 (MXFP4: scales and a 16-byte flag field per 128 x 128
+ * chunk) bytes; 0 for an unknown format. */
 size_t petit_repacked_bytes(int64_t n, int64_t k, int fmt);
 
 /* Bytes of GEMM workspace for this problem on the current device: a device
@@ -153,7 +154,10 @@ petit_status_t petit_repack_nvfp4_f16(const uint8_t* w_packed, const uint8_t* s_
                                       petit_stream_t stream);
 
 /* Same as petit_repack_nvfp4 for MXFP4 scales s_e8m0 [n][k/32] (code 0xFF is
- * not a number and must not occur). */
+ * not a number and must not occur).  Each 128 x 128 chunk also records
+ * whether all its scale codes are at most 128 (scale <= 2, the case for
+ * ordinary weights); the GEMM then decodes its codes with one BF16 multiply
+ * instead of two.  Output of petit_repacked_bytes(n, k, PETIT_FMT_MXFP4). */
 petit_status_t petit_repack_mxfp4(const uint8_t* w_packed, const uint8_t* s_e8m0,
                                   uint8_t* rep_out, int64_t n, int64_t k,
                                   petit_stream_t stream);

@@ -45,7 +45,8 @@ def test_host_only_entry_points(lib):
         assert lib.petit_status_string(s)
     assert lib.petit_status_string(99) == b"unknown status"
     assert lib.petit_repacked_bytes(8192, 8192, 0) == 8192 * 4096 + 8192 * 512
-    assert lib.petit_repacked_bytes(8192, 8192, 1) == 8192 * 4096 + 8192 * 256
+    # MXFP4: codes, scales and a 16-byte flag field per 128 x 128 chunk
+    assert lib.petit_repacked_bytes(8192, 8192, 1) == 8192 * 4096 + 8192 * 256 + 64 * 64 * 16
     assert lib.petit_repacked_bytes(8192, 8192, 7) == 0
     assert lib.petit_nvfp4_global_scale(ctypes.c_float(2688.0)) == 1.0
 

@@ -54,6 +54,27 @@ def test_one_hot_is_bit_exact(cuda_lib, fmt, m, n, k):
     assert np.all((got == expect) | (zero & ((got & 0x7FFF) == 0)))
 
 
+@pytest.mark.parametrize("m", [16, 200])
+def test_mxfp4_one_and_two_multiply_chunks_one_hot(cuda_lib, m):
+    """MXFP4 weights whose second 128-row tile is scaled by 2^20: its chunks
+    hold E8M0 codes above 128 and take the two-multiply decode, the others
+    the one-multiply decode.  One-hot activations make C bit-exact to Wq."""
+    n, k = 384, 1024
+    w = synth.weights(n, k, seed=15)
+    w[128:256] *= 2.0 ** 20                     # exact in BF16
+    codes, scales, rep = _prep(cuda_lib, w, "mxfp4")
+    assert (scales[128:256] > 128).any() and (scales[:128] <= 128).all()
+    rng = np.random.default_rng(m)
+    cols = rng.integers(0, k, m)
+    a = synth.one_hot_activations(m, k, cols).cuda()
+    c = _gemm(cuda_lib, a, rep, n, "mxfp4", 1.0)
+    torch.cuda.synchronize()
+    expect = ogemm.dequantize_bf16_bits(codes, scales, "mxfp4")[:, cols].T
+    got = bf16_bits(c)
+    zero = (expect & 0x7FFF) == 0
+    assert np.all((got == expect) | (zero & ((got & 0x7FFF) == 0)))
+
+
 @pytest.mark.parametrize("m", [1, 2, 3, 5, 8, 16, 17, 33, 64, 65, 100, 128, 255, 256, 300])
 def test_nvfp4_parity_ragged_m(cuda_lib, m):
     n, k = 1024, 1024

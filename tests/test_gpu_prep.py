@@ -48,16 +48,27 @@ def test_repack_dequant_bitexact(cuda_lib, fmt, n, k):
     codes[5, :16] = np.arange(16)
     wp, sp = to_device_packed(codes, scales)
     rep = cuda_lib.repack(wp, sp, fmt)
-    assert rep.numel() == n * k // 2 + scales.size
+    nchunks = (n // 128) * (k // 128)
+    flag_bytes = 16 if fmt == "mxfp4" else 0      # MXFP4: per-chunk flag field
+    assert rep.numel() == n * k // 2 + scales.size + nchunks * flag_bytes
     # the repack permutes bits inside 32-bit code words and moves scale bytes:
     # the number of set bits and the multiset of scale bytes are kept
-    r = rep.cpu().numpy()
+    sbytes = 1024 if fmt == "nvfp4" else 512
+    r = rep.cpu().numpy().reshape(nchunks, 8192 + sbytes + flag_bytes)
     packed = quantize.pack_codes(codes)
     popcount = lambda x: int(np.unpackbits(np.ascontiguousarray(x).view(np.uint8)).sum())
-    assert popcount(r) == popcount(packed) + popcount(scales)
-    chunk = 8192 + (1024 if fmt == "nvfp4" else 512)
-    scale_part = r.reshape(-1, chunk)[:, 8192:]
+    assert popcount(r[:, : 8192 + sbytes]) == popcount(packed) + popcount(scales)
+    scale_part = r[:, 8192 : 8192 + sbytes]
     assert sorted(scale_part.reshape(-1).tolist()) == sorted(scales.reshape(-1).tolist())
+    if fmt == "mxfp4":
+        # flag byte 0: every E8M0 code of the (128-row tile, 128-k stage)
+        # chunk is <= 128; bytes 1..15 zero.  Chunks are tile-major.
+        blocks = scales.reshape(n // 128, 128, k // 128, 4)
+        expect_flag = (blocks <= 128).all(axis=(1, 3)).reshape(-1).astype(np.uint8)
+        np.testing.assert_array_equal(r[:, 8192 + sbytes], expect_flag)
+        assert not r[:, 8192 + sbytes + 1 :].any()
+        if n >= 256:   # row 1's huge values make the first tile take the two-multiply decode
+            assert expect_flag.any() and not expect_flag.all()
     out = cuda_lib.dequant(rep, n, k, fmt)
     torch.cuda.synchronize()
     expect = gemm.dequantize_bf16_bits(codes, scales, fmt)
@@ -87,5 +98,22 @@ def test_dequant_mx_scale_range(cuda_lib):
     scales = rng.integers(7, 248, (n, k // 32)).astype(np.uint8)
     wp, sp = to_device_packed(codes, scales)
     rep = cuda_lib.repack(wp, sp, "mxfp4")
+    got = bf16_bits(cuda_lib.dequant(rep, n, k, "mxfp4"))
+    np.testing.assert_array_equal(got, gemm.dequantize_bf16_bits(codes, scales, "mxfp4"))
+
+
+def test_dequant_mx_fast_path_scale_range(cuda_lib):
+    """E8M0 codes 0..128 (every chunk takes the one-multiply decode), with
+    the boundary codes 0 (2^-127) and 128 (2^1) in every chunk."""
+    n, k = 256, 128 * 8
+    rng = np.random.default_rng(13)
+    codes = rng.integers(0, 16, (n, k)).astype(np.uint8)
+    scales = rng.integers(0, 129, (n, k // 32)).astype(np.uint8)
+    scales[::7, ::4] = 0
+    scales[3::7, 1::4] = 128
+    wp, sp = to_device_packed(codes, scales)
+    rep = cuda_lib.repack(wp, sp, "mxfp4")
+    r = rep.cpu().numpy().reshape(-1, 8192 + 512 + 16)
+    assert r[:, 8192 + 512].all()
     got = bf16_bits(cuda_lib.dequant(rep, n, k, "mxfp4"))
     np.testing.assert_array_equal(got, gemm.dequantize_bf16_bits(codes, scales, "mxfp4"))
