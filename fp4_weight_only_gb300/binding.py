@@ -6,6 +6,7 @@ stream.  If the library cannot be built or loaded, :func:`load` raises --
 there is no CPU fallback.
 """
 
+import contextlib
 import ctypes
 import functools
 import os
@@ -29,6 +30,7 @@ STATUS = {
     5: "PETIT_ERR_ARCH",
     6: "PETIT_ERR_CUDA",
     7: "PETIT_ERR_TIMEOUT",
+    8: "PETIT_ERR_BOUNDS",
 }
 
 _lib = None
@@ -70,6 +72,8 @@ SIGNATURES = {
                                                  _c_p, _c_sz, _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_sz, _c_p]),
     "petit_set_tile_config": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "petit_bounds_checking": (ctypes.c_int, []),
+    "petit_check_set_limits": (ctypes.c_int, [_c_i64, _c_i64]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
 }
 
@@ -80,6 +84,15 @@ class PetitError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
+def _open(path):
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load(build=True):
     """Build (if stale) and load the CUDA library; raises on failure."""
     global _lib
@@ -87,14 +100,36 @@ def load(build=True):
         return _lib
     with _lock:
         if _lib is None:
-            path = _build.build() if build else _build.LIB
-            lib = ctypes.CDLL(path)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = lib
+            _lib = _open(_build.build() if build else _build.LIB)
     return _lib
+
+
+_check_lib = None
+
+
+def load_check(build=True):
+    """Build (if stale) and load the bounds-checking build of the library
+    (``_petit_check.so``: same API; the GEMM kernel checks every buffer
+    index and copy and reports a failed check as PETIT_ERR_BOUNDS)."""
+    global _check_lib
+    with _lock:
+        if _check_lib is None:
+            _check_lib = _open(_build.build_check() if build else _build.CHECK_LIB)
+    return _check_lib
+
+
+@contextlib.contextmanager
+def bounds_checked():
+    """Inside the block every call of this module goes through the
+    bounds-checking build (process-wide; not for concurrent use)."""
+    global _lib
+    chk = load_check()
+    prev = load()
+    _lib = chk
+    try:
+        yield chk
+    finally:
+        _lib = prev
 
 
 def lib_path():

@@ -4,6 +4,11 @@ Each ``csrc/*.cu`` file is compiled in parallel with nvcc into ``_build/``
 and linked into one shared library next to this file (CUDA runtime linked
 statically; the driver API is reached through the runtime's entry-point
 query, so the library loads without libcuda on a machine with no GPU).
+
+``build_check()`` makes the bounds-checking build ``_petit_check.so`` (same
+sources and API, compiled with ``-DPETIT_CHECK_BOUNDS`` into
+``_build_check/``): the GEMM kernel checks every buffer index and copy
+before use and reports a failed check as a status instead of faulting.
 """
 
 import os
@@ -16,6 +21,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "_petit.so")
+BUILD_CHECK = os.path.join(HERE, "_build_check")
+CHECK_LIB = os.path.join(HERE, "_petit_check.so")
+CHECK_FLAGS = ["-DPETIT_CHECK_BOUNDS"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 
@@ -37,23 +45,23 @@ def _inputs():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force=False, verbose=False, extra_flags=()):
+def build(force=False, verbose=False, extra_flags=(), lib=LIB, build_dir=BUILD):
     """Compile and link the library if any input is newer than it."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
@@ -69,15 +77,21 @@ def build(force=False, verbose=False, extra_flags=()):
             print(text, file=sys.stderr)
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_check(force=False, verbose=False):
+    """The bounds-checking build, ``_petit_check.so``."""
+    return build(force, verbose, CHECK_FLAGS, CHECK_LIB, BUILD_CHECK)
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB)
+    check = "--check" in sys.argv
+    fn = build_check if check else build
+    print(fn(force="--force" in sys.argv, verbose=True))

@@ -240,6 +240,7 @@ const char* petit_status_string(petit_status_t s) {
     case PETIT_ERR_ARCH: return "device is not sm_103 (GB300)";
     case PETIT_ERR_CUDA: return "CUDA runtime error";
     case PETIT_ERR_TIMEOUT: return "device-side wait timed out";
+    case PETIT_ERR_BOUNDS: return "device-side index check failed";
   }
   return "unknown status";
 }
@@ -408,6 +409,12 @@ petit_status_t petit_set_tile_config(int bn, int ku) {
   return petit::set_tile_override(bn, ku) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
 }
 
+int petit_bounds_checking(void) { return petit::bounds_checking() ? 1 : 0; }
+
+petit_status_t petit_check_set_limits(int64_t weight_bytes, int64_t c_elems) {
+  return petit::set_check_limits(weight_bytes, c_elems) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
+}
+
 petit_status_t petit_get_device_status(void* workspace, size_t workspace_bytes,
                                        petit_stream_t stream) {
   if (!workspace || workspace_bytes < petit::kWsHeaderBytes) return PETIT_ERR_INVALID_ARG;
@@ -425,6 +432,7 @@ petit_status_t petit_get_device_status(void* workspace, size_t workspace_bytes,
   const size_t clear = workspace_bytes >= counters_end ? counters_end : sizeof(word);
   if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
     return PETIT_ERR_CUDA;
+  if (word & petit::kStatusBounds) return PETIT_ERR_BOUNDS;
   return (word & petit::kStatusTimeout) ? PETIT_ERR_TIMEOUT : PETIT_ERR_CUDA;
 }
 

@@ -33,6 +33,15 @@
 //   the FP4 chunk and the activation tile.
 // * Every wait is bounded; a wait that runs out records a timeout in the
 //   workspace status word and the CTA shuts down cleanly.
+// * Bounds-checking build (-DPETIT_CHECK_BOUNDS, a separate library): every
+//   global-memory access, bulk or tensor copy and shared- or tensor-memory
+//   buffer index of the kernel is checked against its buffer's extent first.
+//   A failed check skips the access (a skipped copy still arrives on its
+//   barrier, so no wait is left hanging on it), marks the CTA aborted and
+//   the CTA shuts down as after a timeout; thread 0 then records
+//   kStatusBounds in the workspace status word.  No trap, no assert.  In the
+//   normal build each check is the constant true and its operand is not
+//   compiled.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -55,6 +64,20 @@ constexpr int kDeqGroupWarps = 4;   // one dequantiser group: a warp per lane qu
 constexpr int kMaxMmaThreads = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kFixBatch = 2;   // split-tile contributors whose partials are loaded together
+// bits of a CTA's abort flag (shared memory)
+constexpr int kAbortTimeout = 1;
+constexpr int kAbortBounds = 2;
+
+#ifdef PETIT_CHECK_BOUNDS
+// A failed index check aborts the CTA.
+__device__ __forceinline__ bool check_ok(bool ok, volatile int* abort) {
+  if (!ok) atomicOr(const_cast<int*>(abort), kAbortBounds);
+  return ok;
+}
+#define PETIT_CHECK(cond) check_ok((cond), abort_flag)
+#else
+#define PETIT_CHECK(cond) true
+#endif
 
 struct Params {
   const uint8_t* rep;
@@ -78,6 +101,11 @@ struct Params {
   int32_t row_off[kMaxGroups + 1];    // group g: activation / output rows
   int32_t tile_base[kMaxGroups + 1];  // group g: first tile
   float group_alpha[kMaxGroups];      // epilogue factor per group
+#ifdef PETIT_CHECK_BOUNDS
+  int64_t chk_rep_bytes;   // bytes of each group's repacked weights the kernel may read
+  int64_t chk_c_elems;     // elements of C it may write
+  int32_t chk_a_rows;      // activation rows (the tensor map's row extent)
+#endif
 };
 
 // Split tiles.  A contributor stores its FP32 partial and then arrives on
@@ -193,6 +221,24 @@ struct WeightStream {
   __device__ __forceinline__ void issue(const Params& p, uint64_t policy) {
     mbar_arrive_expect_tx(full0 + bar, kBytes);
     bulk_g2s(dst, src, kBytes, full0 + bar, policy);
+    advance(p);
+  }
+  // bounds-checking build: the copy's source lies inside its group's
+  // repacked weights and its destination inside the weight ring
+  __device__ __forceinline__ bool in_bounds(const Params& p) const {
+#ifdef PETIT_CHECK_BOUNDS
+    if (cur.g < 0 || cur.g >= p.num_groups) return false;
+    const uint8_t* base = p.rep + cur.g * p.rep_stride;
+    return src >= base && src + kBytes <= base + p.chk_rep_bytes && dst >= dst0 &&
+           dst + kBytes <= dst0 + static_cast<uint32_t>(stages) * kBytes &&
+           bar < 8u * static_cast<uint32_t>(stages);
+#else
+    return true;
+#endif
+  }
+  // a copy that failed its check: the stage's barrier completes without data
+  __device__ __forceinline__ void skip(const Params& p) {
+    mbar_arrive(full0 + bar);
     advance(p);
   }
 };
@@ -337,8 +383,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t U = p.units;
-  const int64_t P = p.num_ctas;
+  [[maybe_unused]] const int64_t P = p.num_ctas;   // (index checks)
   const int64_t cta = blockIdx.x;
   const int64_t u0 = cta_lo(p, blockIdx.x);
   const int64_t u1 = cta_lo(p, blockIdx.x + 1);
@@ -390,7 +435,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 
   // a wait that runs out records the abort in shared memory only; thread 0
   // (which has passed the grid dependency wait) reports it at the end
-  auto fail = [&]() { *abort_flag = 1; };
+  auto fail = [&]() { atomicOr(const_cast<int*>(abort_flag), kAbortTimeout); };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (mbar_wait_bounded(smem_u32(bar), parity, p.timeout_ns, abort_flag)) return true;
     if (!*abort_flag) fail();
@@ -433,11 +478,26 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       for (uint32_t spin = 0; wi < nu || xi < nu;) {
         bool progress = false;
         if (wi < nu && mbar_test_wait(wfree0 + ws.bar, ws.ph ^ 1u)) {
+          if (!PETIT_CHECK(ws.in_bounds(p))) {
+            ws.skip(p);
+            ++wi;
+            break;
+          }
           ws.issue(p, policy);
           ++wi;
           progress = true;
         }
         if (xi < nu && mbar_test_wait(mdone0 + xbar, xph ^ 1u)) {
+          // the box's first row and slab lie inside A (rows past its end
+          // read as zeros) and its destination inside the activation ring
+          if (!PETIT_CHECK(xrow >= 0 && xrow < p.chk_a_rows && xk >= 0 &&
+                           xk + 2 * KU <= 2 * KU * ks && xdst >= xdst0 &&
+                           xdst + C::kABytes <= xdst0 + C::kXStages * C::kABytes &&
+                           xbar < 8u * C::kXStages)) {
+            mbar_arrive(xfull0 + xbar);
+            ++xi;
+            break;
+          }
           mbar_arrive_expect_tx(xfull0 + xbar, C::kABytes);
           tma_load_3d(xdst, &tmap_a, 0, xrow, xk, xfull0 + xbar);
           ++xi;
@@ -518,6 +578,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             break;
           }
           tc_fence_after();
+          if (!PETIT_CHECK(st >= 0 && st < C::kXStages && b >= 0 && b < C::kNumA && d >= 0 &&
+                           d < C::kNumD)) {
+            ok = false;
+            break;
+          }
           const uint32_t a_smem = smem_u32(sm_a + st * C::kABytes);
           const uint32_t d_tmem = tmem + C::kDColBase + (t * C::kNumD + d) * BN;
           const uint32_t a_tmem = tmem + b * C::kAColsPerUnit;
@@ -572,7 +637,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       WeightStream<FMT, BN, KU> ws;
       ws.init(p, tile0_32, ku0_32, ks32, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
       const uint64_t policy = p.weights_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
-      for (int64_t j = 0; j < u1 - u0 && j < C::kWStages; ++j) ws.issue(p, policy);
+      for (int64_t j = 0; j < u1 - u0 && j < C::kWStages; ++j) {
+        if (PETIT_CHECK(ws.in_bounds(p))) ws.issue(p, policy);
+        else ws.skip(p);   // every first-ring stage completes: the producer counts them
+      }
       // The CTAs with the highest indices take their SMs last (as the
       // previous kernel's CTAs leave them); a CTA of the lower half pulls the
       // first ring of weight chunks of its partner in the upper half into
@@ -584,6 +652,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         WeightStream<FMT, BN, KU> pw;
         pw.init(p, pu0 / ks32, pu0 % ks32, ks32, 0, 0, C::kWStages);
         for (int32_t j = 0; j < pn && j < C::kWStages; ++j) {
+          if (!PETIT_CHECK(pw.in_bounds(p))) break;
           bulk_prefetch_l2(pw.src, WeightStream<FMT, BN, KU>::kBytes);
           pw.advance(p);
         }
@@ -627,11 +696,15 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         c_first = cta_of_unit(p, tile * KS);
         c_last = cta_of_unit(p, (tile + 1) * KS - 1);
         first_slot = 2 * c_first + (cta_lo(p, static_cast<int32_t>(c_first)) / KS == tile ? 0 : 1);
+        if (!PETIT_CHECK(c_first >= 0 && c_first <= c_last && c_last < P && c_first < kMaxCtas &&
+                         first_slot >= 0 && first_slot < 2 * P))
+          break;
         ctr = &p.counters[c_first];
         // first look while the segment's MMAs run
         if (last_seg && epi_tid == 0)
           *epi_flag = ld_acquire_gpu(ctr) == static_cast<uint32_t>(c_last - c_first);
       }
+      if (!PETIT_CHECK(d >= 0 && d < C::kNumD)) break;
       if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
       // issuer t wrote its accumulator iff the segment holds a unit with
@@ -674,6 +747,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
       const int64_t slot = 2 * cta + (tile == first_tile_of_cta ? 0 : 1);
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
+      // (a partial slot holds BN x 128 floats; r < 128)
+      if (!full_tile && !PETIT_CHECK(slot >= 0 && slot < 2 * P)) break;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         // the contributing accumulators, added in issuer order
@@ -695,7 +770,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-            if (mrow < g_rows) c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * __uint_as_float(v[j]));
+            if (mrow < g_rows && PETIT_CHECK(ncol < p.n && (c_g - p.c) + mrow * p.n + ncol <
+                                                             p.chk_c_elems))
+              c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * __uint_as_float(v[j]));
           }
         } else {
 #pragma unroll
@@ -752,6 +829,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
                 const int64_t c = cb + x;
                 if (c <= c_last) {
                   const int64_t cs = c == c_first ? first_slot : 2 * c;
+                  if (!PETIT_CHECK(cs >= 0 && cs < 2 * P)) continue;
                   const float* src =
                       p.partials + static_cast<size_t>(cs) * (BN * kTileN) + c0 * kTileN + r;
 #pragma unroll
@@ -769,7 +847,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
-              if (mrow < g_rows) c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * acc[j]);
+              if (mrow < g_rows && PETIT_CHECK(ncol < p.n && (c_g - p.c) + mrow * p.n + ncol <
+                                                               p.chk_c_elems))
+                c_g[mrow * p.n + ncol] = out_bits<FMT>(alpha * acc[j]);
             }
           }
         }
@@ -802,6 +882,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     int st2 = (i0 - C::kNumA) % C::kXStages;
     uint32_t ph2 = ((i0 - C::kNumA) / C::kXStages) & 1;
     for (int32_t i = grp; i < nu; i += G) {
+      if (!PETIT_CHECK(st >= 0 && st < C::kWStages && b >= 0 && b < C::kNumA && st2 >= 0 &&
+                       st2 < C::kXStages))
+        break;
       if (!wait(&wfull[st], ph)) break;
       bool ok = true;
 #pragma unroll
@@ -888,7 +971,9 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     constexpr int kCols = BN / kFixGroups;               // activation rows per group
     constexpr int kLd = kCols >= 16 ? 16 : 4;            // columns per tensor-memory load
     const int fg = warp >> 2;
-    if (fg < kFixGroups && !*abort_flag) {
+    if (fg < kFixGroups && !*abort_flag &&
+        PETIT_CHECK(f.d >= 0 && f.d < C::kNumD && f.c_first >= 0 && f.c_first <= cta &&
+                    cta <= f.c_last && f.c_last < P && f.first_slot >= 0 && f.first_slot < 2 * P)) {
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase +
@@ -945,7 +1030,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 #pragma unroll
         for (int j = 0; j < kLd; ++j) {
           const int64_t mrow = f.row0 + m0 + j;
-          if (mrow < f.g_rows) f.c_g[mrow * p.n + f.col0 + r] = out_bits<FMT>(f.alpha * acc[j]);
+          if (mrow < f.g_rows &&
+              PETIT_CHECK(f.col0 + r < p.n &&
+                          (f.c_g - p.c) + mrow * p.n + f.col0 + r < p.chk_c_elems))
+            f.c_g[mrow * p.n + f.col0 + r] = out_bits<FMT>(f.alpha * acc[j]);
         }
       }
     }
@@ -956,7 +1044,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   // a wait that ran out anywhere in the CTA is reported by thread 0, which
   // has passed the grid dependency wait
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
+  if (threadIdx.x == 0 && *abort_flag)
+    atomicOr(p.status, (*abort_flag & kAbortBounds) ? kStatusBounds : kStatusTimeout);
 }
 
 template <int FMT, int BN, int KU>
@@ -1054,12 +1143,31 @@ void plan_bounds(GemmPlan& pl, double late_ns) {
 }
 
 std::atomic<int> g_tile_override{0};   // bn | ku << 16, or 0: the planner decides
+// bounds-checking build: extents the checks use in place of the true ones
+// (negative: the true extent)
+std::atomic<int64_t> g_check_weight_bytes{-1};
+std::atomic<int64_t> g_check_c_elems{-1};
 
 double late_start_ns() { return kLateStartNs; }
 
 }  // namespace
 
 int tile_override() { return g_tile_override.load(std::memory_order_relaxed); }
+
+bool bounds_checking() {
+#ifdef PETIT_CHECK_BOUNDS
+  return true;
+#else
+  return false;
+#endif
+}
+
+bool set_check_limits(int64_t weight_bytes, int64_t c_elems) {
+  if (!bounds_checking()) return false;
+  g_check_weight_bytes.store(weight_bytes);
+  g_check_c_elems.store(c_elems);
+  return true;
+}
 
 bool set_tile_override(int bn, int ku) {
   if (bn == 0 && ku == 0) {
@@ -1174,6 +1282,18 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   }
   for (int g = 0; g < pl.num_groups; ++g)
     prm.group_alpha[g] = a.group_alpha ? a.group_alpha[g] : a.alpha;
+#ifdef PETIT_CHECK_BOUNDS
+  {
+    const int64_t chunk = pl.fmt == kMXFP4 ? FmtTraits<kMXFP4>::kChunkBytes
+                                           : FmtTraits<kNVFP4>::kChunkBytes;
+    const int64_t wb = static_cast<int64_t>(pl.n_tiles) * pl.k_stages * chunk;
+    const int64_t ce = static_cast<int64_t>(pl.row_off[pl.num_groups]) * a.n;
+    const int64_t lw = g_check_weight_bytes.load(), lc = g_check_c_elems.load();
+    prm.chk_rep_bytes = lw >= 0 && lw < wb ? lw : wb;
+    prm.chk_c_elems = lc >= 0 && lc < ce ? lc : ce;
+    prm.chk_a_rows = pl.row_off[pl.num_groups];
+  }
+#endif
   if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);
   if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream, a.device);
   return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);

@@ -8,7 +8,8 @@
 
 namespace petit {
 
-constexpr uint32_t kStatusTimeout = 1u;  // bit in the workspace status word
+constexpr uint32_t kStatusTimeout = 1u;  // bits in the workspace status word
+constexpr uint32_t kStatusBounds = 2u;   // (bounds-checking build only)
 
 // Workspace: [0, 256) status word and reserved; [256, 4352) split-tile
 // arrival counters (u32), one per CTA index -- a split tile counts on the
@@ -61,6 +62,12 @@ GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
 // Returns false for any other pair.
 bool set_tile_override(int bn, int ku);
 int tile_override();   // bn | ku << 16, or 0
+// Whether this library is the bounds-checking build; in it, the extents the
+// GEMM kernel's checks use (weight bytes per group, elements of C) may be
+// lowered for tests (negative: the true extent).  Returns false in the
+// normal build.
+bool bounds_checking();
+bool set_check_limits(int64_t weight_bytes, int64_t c_elems);
 // row_off: num_groups + 1 non-decreasing offsets starting at 0
 GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
                       int num_sms);

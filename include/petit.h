@@ -68,7 +68,8 @@ typedef enum petit_status {
   PETIT_ERR_WORKSPACE = 4,         /* workspace missing or too small */
   PETIT_ERR_ARCH = 5,              /* current device is not sm_103 */
   PETIT_ERR_CUDA = 6,              /* a CUDA runtime call failed */
-  PETIT_ERR_TIMEOUT = 7            /* a bounded device-side wait ran out */
+  PETIT_ERR_TIMEOUT = 7,           /* a bounded device-side wait ran out */
+  PETIT_ERR_BOUNDS = 8             /* an index check failed (bounds-checking build only) */
 } petit_status_t;
 
 typedef enum petit_format {
@@ -304,12 +305,37 @@ petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uint8_t* rep,
  * other host threads.  Errors: PETIT_ERR_INVALID_ARG for any other pair. */
 petit_status_t petit_set_tile_config(int bn, int ku);
 
+/* ------------------------------------------------- bounds-checking build */
+
+/* The library also builds as _petit_check.so with every global-memory
+ * access, bulk and tensor copy and shared- or tensor-memory buffer index of
+ * the GEMM kernel checked against its buffer's extent before use (a debug
+ * aid for the illegal-address failures a wrong index or copy coordinate
+ * gives: CUTLASS FP4 article, sections 5.1 and 7).  A failed check skips
+ * the access, stops the CTA cleanly and records PETIT_ERR_BOUNDS for
+ * petit_get_device_status(); no trap, no device assert.  Same API, slower.
+ *
+ * petit_bounds_checking(): 1 in the bounds-checking build, else 0. */
+int petit_bounds_checking(void);
+
+/* Bounds-checking build only: the checks of later GEMM launches in this
+ * process use at most `weight_bytes` bytes of each group's repacked weights
+ * and `c_elems` elements of C as the extents (a negative value: the true
+ * extent), so a test can make a check fail while every access that does
+ * happen stays inside its real buffer.  Not thread-safe with respect to
+ * concurrent GEMM calls.  The normal build returns PETIT_ERR_INVALID_ARG and
+ * changes nothing. */
+petit_status_t petit_check_set_limits(int64_t weight_bytes, int64_t c_elems);
+
 /* --------------------------------------------------------- error reporting */
 
 /* Waits for `stream`, then reads the status word the kernels keep at the
  * start of `workspace` (device, workspace_bytes >= 256).  Returns PETIT_OK,
  * PETIT_ERR_TIMEOUT (a bounded wait ran out in some earlier call on this
- * workspace) or PETIT_ERR_CUDA.  When the word is not zero it is cleared,
+ * workspace), PETIT_ERR_BOUNDS (in the bounds-checking build of the
+ * library, _petit_check.so: a kernel found an index outside its buffer,
+ * skipped that access and stopped) or PETIT_ERR_CUDA.  When the word is not
+ * zero it is cleared,
  * together with the split-tile arrival counters (bytes 256..4351, when
  * workspace_bytes covers them) that a kernel which stopped early may have
  * left raised; the workspace can then be used again without re-zeroing it.

@@ -41,8 +41,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_host_only_entry_points(lib):
     assert lib.petit_layout_version() >= 1
-    for s in range(8):
+    for s in range(9):
         assert lib.petit_status_string(s)
+    assert lib.petit_status_string(8) == b"device-side index check failed"
     assert lib.petit_status_string(99) == b"unknown status"
     assert lib.petit_repacked_bytes(8192, 8192, 0) == 8192 * 4096 + 8192 * 512
     # MXFP4: codes, scales and a 16-byte flag field per 128 x 128 chunk
@@ -101,3 +102,18 @@ def test_tile_config_override_validation(lib):
     assert lib.petit_set_tile_config(16, 3) == 1
     assert lib.petit_set_tile_config(256, 1) == 0
     assert lib.petit_set_tile_config(0, 0) == 0
+
+
+def test_bounds_checking_build_loads_and_differs_only_in_checks(lib):
+    """The bounds-checking build (_petit_check.so) has the same ABI; only it
+    accepts test limits for its index checks."""
+    chk = binding.load_check()
+    names = declared_functions()
+    assert not [n for n in names if not hasattr(chk, n)]
+    assert lib.petit_bounds_checking() == 0
+    assert chk.petit_bounds_checking() == 1
+    assert lib.petit_check_set_limits(1024, -1) == 1    # normal build: no checks to limit
+    assert chk.petit_check_set_limits(1024, -1) == 0
+    assert chk.petit_check_set_limits(-1, -1) == 0
+    assert chk.petit_layout_version() == lib.petit_layout_version()
+    assert chk.petit_repacked_bytes(4096, 4096, 1) == lib.petit_repacked_bytes(4096, 4096, 1)
