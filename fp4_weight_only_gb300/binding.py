@@ -72,6 +72,7 @@ SIGNATURES = {
                                                  _c_p, _c_sz, _c_p]),
     "petit_get_device_status": (ctypes.c_int, [_c_p, _c_sz, _c_p]),
     "petit_set_tile_config": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "petit_set_pair_mode": (ctypes.c_int, [ctypes.c_int]),
     "petit_bounds_checking": (ctypes.c_int, []),
     "petit_check_set_limits": (ctypes.c_int, [_c_i64, _c_i64]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
@@ -308,6 +309,14 @@ def set_tile_config(bn=0, ku=0):
     """Force the GEMM tile shape (bn activation rows, ku 128-k chunks per
     unit) for later calls in this process; (0, 0) restores the planner."""
     _check(load().petit_set_tile_config(int(bn), int(ku)), "set_tile_config")
+    workspace_bytes.cache_clear()
+
+
+def set_pair_mode(mode=0):
+    """CTA pairs (cta_group::2) for 128/256-row tiles in later calls of this
+    process: 0 where the planner expects a gain, 1 never, 2 wherever they
+    apply."""
+    _check(load().petit_set_pair_mode(int(mode)), "set_pair_mode")
     workspace_bytes.cache_clear()
 
 

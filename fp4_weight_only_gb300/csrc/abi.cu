@@ -28,16 +28,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DevInfo {
   std::atomic<int> state{0};
   int num_sms = 0;
+  int pair_cap = 0;   // resident CTA pairs of the pair kernels
 };
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;   // only for the first probe of a device
 DevInfo g_dev[kMaxDevices];
 
-// Current device (one cudaGetDevice), its SM count, and whether it is a
-// compute-capability 10.3 part (the only code this library contains is
-// sm_103a).
-petit_status_t current_device(int* sms, int* dev_out = nullptr) {
+// Current device (one cudaGetDevice), its SM count, how many CTA pairs of
+// the pair kernels it holds at once, and whether it is a compute-capability
+// 10.3 part (the only code this library contains is sm_103a).
+petit_status_t current_device(int* sms, int* dev_out = nullptr, int* pair_cap = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -58,11 +59,13 @@ petit_status_t current_device(int* sms, int* dev_out = nullptr) {
       }
       d.num_sms = n;
       st = (major == 10 && minor == 3) ? 1 : 2;
+      d.pair_cap = st == 1 ? petit::pair_capacity() : 0;
       d.state.store(st, std::memory_order_release);
     }
   }
   if (sms) *sms = d.num_sms;
   if (dev_out) *dev_out = dev;
+  if (pair_cap) *pair_cap = d.pair_cap;
   return st == 1 ? PETIT_OK : PETIT_ERR_ARCH;
 }
 
@@ -163,12 +166,15 @@ petit_status_t gemm_common(int fmt, const void* A, const uint8_t* rep, float alp
   if (!ws) return PETIT_ERR_WORKSPACE;
   if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
   int sms = 0, dev = 0;
-  if (petit_status_t st = current_device(&sms, &dev)) return st;
-  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, fmt, sms);
+  int pair_cap = 0;
+  if (petit_status_t st = current_device(&sms, &dev, &pair_cap)) return st;
+  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, fmt, sms, pair_cap);
   if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
-  if (petit_status_t st = cached_a_map(&map, A, m, k, plan.bn, plan.ku, fmt == kNVFP4F16, dev))
+  // (CTA pairs: each CTA's activation box holds half of a tile's rows)
+  if (petit_status_t st = cached_a_map(&map, A, m, k, plan.pair ? plan.bn / 2 : plan.bn, plan.ku,
+                                       fmt == kNVFP4F16, dev))
     return st;
   petit::GemmArgs args{A, rep, C, m, n, k, alpha, static_cast<uint8_t*>(ws), kGemmTimeoutNs};
   args.device = dev;
@@ -210,13 +216,16 @@ petit_status_t moe_common(int fmt, const void* A, const uint8_t* rep, const floa
   if (!ws) return PETIT_ERR_WORKSPACE;
   if (!aligned16(ws)) return PETIT_ERR_MISALIGNED;
   int sms = 0, dev = 0;
-  if (petit_status_t st = current_device(&sms, &dev)) return st;
+  int pair_cap = 0;
+  if (petit_status_t st = current_device(&sms, &dev, &pair_cap)) return st;
   const petit::GemmPlan plan =
-      petit::plan_grouped(off, static_cast<int>(num_experts), n, k, fmt, sms);
+      petit::plan_grouped(off, static_cast<int>(num_experts), n, k, fmt, sms, pair_cap);
   if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < plan.ws.total) return PETIT_ERR_WORKSPACE;
   CUtensorMap map;
-  if (petit_status_t st = cached_a_map(&map, A, rows, k, plan.bn, plan.ku, false, dev)) return st;
+  if (petit_status_t st = cached_a_map(&map, A, rows, k, plan.pair ? plan.bn / 2 : plan.bn,
+                                       plan.ku, false, dev))
+    return st;
   petit::GemmArgs args{A, rep, C, rows, n, k, alphas[0], static_cast<uint8_t*>(ws), kGemmTimeoutNs};
   args.device = dev;
   args.rep_stride = static_cast<int64_t>(petit_repacked_bytes(n, k, fmt));
@@ -258,8 +267,9 @@ size_t petit_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int fmt) {
   if (m < 1 || m > kMaxDim || check_tiled_shape(n, k) != PETIT_OK) return 0;
   if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4 && fmt != PETIT_FMT_NVFP4_F16) return 0;
   int sms = 0;
-  if (current_device(&sms) != PETIT_OK) return 0;
-  return petit::plan_gemm(m, n, k, fmt, sms).ws.total;
+  int pair_cap = 0;
+  if (current_device(&sms, nullptr, &pair_cap) != PETIT_OK) return 0;
+  return petit::plan_gemm(m, n, k, fmt, sms, pair_cap).ws.total;
 }
 
 size_t petit_moe_workspace_bytes(const int64_t* expert_offsets, int64_t num_experts, int64_t n,
@@ -268,8 +278,11 @@ size_t petit_moe_workspace_bytes(const int64_t* expert_offsets, int64_t num_expe
     return 0;
   if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return 0;
   int sms = 0;
-  if (current_device(&sms) != PETIT_OK) return 0;
-  return petit::plan_grouped(expert_offsets, static_cast<int>(num_experts), n, k, fmt, sms).ws.total;
+  int pair_cap = 0;
+  if (current_device(&sms, nullptr, &pair_cap) != PETIT_OK) return 0;
+  return petit::plan_grouped(expert_offsets, static_cast<int>(num_experts), n, k, fmt, sms,
+                             pair_cap)
+      .ws.total;
 }
 
 petit_status_t petit_moe_gemm_bf16_mxfp4(const void* A, const uint8_t* rep,
@@ -409,6 +422,10 @@ petit_status_t petit_set_tile_config(int bn, int ku) {
   return petit::set_tile_override(bn, ku) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
 }
 
+petit_status_t petit_set_pair_mode(int mode) {
+  return petit::set_pair_mode(mode) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
+}
+
 int petit_bounds_checking(void) { return petit::bounds_checking() ? 1 : 0; }
 
 petit_status_t petit_check_set_limits(int64_t weight_bytes, int64_t c_elems) {
@@ -482,8 +499,9 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
   if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(A) || !aligned16(rep) || !aligned16(C)) return PETIT_ERR_MISALIGNED;
   int sms = 0;
-  if (petit_status_t st = current_device(&sms)) return st;
-  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, kNVFP4, sms);
+  int pair_cap = 0;
+  if (petit_status_t st = current_device(&sms, nullptr, &pair_cap)) return st;
+  const petit::GemmPlan plan = petit::plan_gemm(m, n, k, kNVFP4, sms, pair_cap);
   if (plan.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
   if (plan.ws.total > kNoAllocScratchBytes) return PETIT_ERR_WORKSPACE;  // problem too large
   int dev = 0;
@@ -509,7 +527,9 @@ extern "C" petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uin
   // every check that can fail comes before the first enqueue
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
-  if (petit_status_t st = encode_a_map(&map, A, m, k, plan.bn, plan.ku)) return st;
+  if (petit_status_t st =
+          encode_a_map(&map, A, m, k, plan.pair ? plan.bn / 2 : plan.bn, plan.ku))
+    return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the arrival counters must start at zero; the array
   // keeps whatever the previous call left in it

@@ -184,6 +184,7 @@ struct WeightStream {
   const uint8_t* src;
   int32_t KS;            // units per tile
   int32_t ku;            // unit index inside the tile
+  int32_t wmul, wadd;    // weight tile of work tile nt: nt * wmul + wadd (CTA pairs: 2 nt + rank)
   TileCursor cur;
   uint32_t dst, dst0;    // shared-memory stage, first stage
   uint32_t bar, full0;   // stage * 8, address of the stage-0 full barrier
@@ -192,11 +193,15 @@ struct WeightStream {
 
   // starting at unit ku of tile `tile`
   __device__ __forceinline__ void init(const Params& p, int32_t tile, int32_t ku0, int32_t ks,
-                                       uint32_t sm_w, uint32_t wfull0, int32_t nstages) {
+                                       uint32_t sm_w, uint32_t wfull0, int32_t nstages,
+                                       int32_t tile_mul = 1, int32_t tile_add = 0) {
     KS = ks;
     ku = ku0;
+    wmul = tile_mul;
+    wadd = tile_add;
     cur = cursor_at<BN>(p, tile);
-    src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, ku * KU, KS * KU);
+    src = p.rep + cur.g * p.rep_stride +
+          chunk_offset<FMT>(cur.nt * wmul + wadd, ku * KU, KS * KU);
     dst = dst0 = sm_w;
     bar = 0;
     full0 = wfull0;
@@ -215,7 +220,7 @@ struct WeightStream {
     if (++ku == KS) {
       ku = 0;
       cursor_next<BN>(p, cur);
-      src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt, 0, KS * KU);
+      src = p.rep + cur.g * p.rep_stride + chunk_offset<FMT>(cur.nt * wmul + wadd, 0, KS * KU);
     }
   }
   __device__ __forceinline__ void issue(const Params& p, uint64_t policy) {
@@ -243,10 +248,16 @@ struct WeightStream {
   }
 };
 
-template <int FMT, int BN, int KU>
+template <int FMT, int BN, int KU, bool PAIR = false>
 struct Cfg {
   using T = FmtTraits<FMT>;
-  static constexpr int kAHalfBytes = BN * 128;                 // one 64-k slab, BN rows
+  // CTA pairs (PAIR): two CTAs of a cluster take adjacent 128-row weight
+  // tiles of the same work tile and one thread of the even CTA issues
+  // cta_group::2 MMAs (M = 256); each CTA holds BN / 2 of the tile's BN
+  // activation rows, so a CTA's activation stage and its share of the L2
+  // activation traffic are halved.
+  static constexpr int kARows = PAIR ? BN / 2 : BN;            // activation rows in this CTA
+  static constexpr int kAHalfBytes = kARows * 128;             // one 64-k slab
   static constexpr int kABytes = 2 * KU * kAHalfBytes;
   static constexpr int kWBytes = KU * T::kChunkBytes;          // codes + scales
   // MMA-issuing threads.  A thread issues one tcgen05.mma per ~65 cycles
@@ -255,7 +266,7 @@ struct Cfg {
   // each into its own accumulator, which the epilogue adds in a fixed order.
   // Three issuers (warps 1, 14, 15 on sub-partitions 1, 2, 3) keep the CTA
   // at 16 warps, four per sub-partition, so each thread may use 128 registers.
-  static constexpr int kMmaThreads = BN <= 32 ? 3 : BN <= 128 ? 2 : 1;
+  static constexpr int kMmaThreads = PAIR ? 1 : BN <= 32 ? 3 : BN <= 128 ? 2 : 1;
   // dequantiser groups (four warps each) taking units round-robin
   static constexpr int kDeqGroups = 2;
   static constexpr int kMmaWarpX = kDeqWarp0 + kDeqGroupWarps * kDeqGroups - 1;  // issuer t>=1: +t
@@ -282,7 +293,9 @@ struct Cfg {
   //     unit i - kNumA, and no later unit sharing that barrier may complete
   //     first.
   static constexpr int kXMult = kMmaThreads == 3 ? 6 : kMmaThreads;
-  static constexpr int kXBudget = BN >= 256 ? 192 * 1024 : (BN <= 32 ? 96 * 1024 : 128 * 1024);
+  static constexpr int kXBudget =
+      PAIR ? (BN >= 256 ? 128 * 1024 : 96 * 1024)
+           : (BN >= 256 ? 192 * 1024 : (BN <= 32 ? 96 * 1024 : 128 * 1024));
   static constexpr int kXStages0 = (kXBudget / kABytes) / kXMult * kXMult;
   static constexpr int kXStages = kXStages0 > 16 ? 16 / kXMult * kXMult : kXStages0;
   static constexpr int kRingBytes = 220 * 1024;
@@ -293,9 +306,11 @@ struct Cfg {
   static constexpr int kNumA = kNumA1 > kXStages ? kXStages / kMmaThreads * kMmaThreads : kNumA1;
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
   static constexpr int kSmemBytes = 1024 + kXStages * kABytes + kWStages * kWBytes + 1024;
+  static constexpr uint32_t kM = PAIR ? 256 : 128;   // MMA M (weight rows of both CTAs)
   static constexpr uint32_t kIdesc =
-      FMT == kNVFP4F16 ? idesc_f16_f32(128, BN) : idesc_bf16_f32(128, BN);
+      FMT == kNVFP4F16 ? idesc_f16_f32(kM, BN) : idesc_bf16_f32(kM, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(!PAIR || (BN >= 128 && KU == 1), "CTA pairs: 128- or 256-row tiles, 128-k units");
   static_assert(kNumA >= 2, "tensor memory");
   static_assert(kDColBase + kMmaThreads * kNumD * BN <= static_cast<int>(kTmemCols),
                 "tensor memory");
@@ -314,7 +329,7 @@ struct Cfg {
   static_assert(2 * kSmemBytes > 228 * 1024, "one CTA per SM");
   // barriers, tensor-memory holder, flags and the deferred fix-up job fit in
   // the 1024 bytes after the rings
-  static_assert((2 * kWStages + 2 * kXStages + kNumA + 2 * kNumD + kMaxMmaThreads + 1) * 8 + 16 +
+  static_assert((2 * kWStages + 3 * kXStages + kNumA + 2 * kNumD + kMaxMmaThreads + 1) * 8 + 16 +
                         sizeof(FixJob) + 16 <= 1024,
                 "barrier region");
 };
@@ -348,15 +363,15 @@ __device__ __forceinline__ int32_t cta_of_unit(const Params& p, int64_t u) {
   return lo;
 }
 
-template <int FMT, int BN, int KU>
-__global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
+template <int FMT, int BN, int KU, bool PAIR>
+__global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_a) {
-  using C = Cfg<FMT, BN, KU>;
+  using C = Cfg<FMT, BN, KU, PAIR>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][BN][128 B]
+  uint8_t* sm_a = smem;                                   // [stage][2*KU slabs][kARows][128 B]
   uint8_t* sm_w = sm_a + C::kXStages * C::kABytes;         // [stage][KU chunks]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm_w + C::kWStages * C::kWBytes);
   // Weights and activations of a unit share a stage index but have their
@@ -375,7 +390,10 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
   uint64_t* dempty = dfull + C::kNumD;
   uint64_t* fin = dempty + C::kNumD;   // one per MMA issuer
   uint64_t* epi_bar = fin + kMaxMmaThreads;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  // CTA pairs: xpeer[s] (even CTA) -- the odd CTA's half of activation stage
+  // s has landed (forwarded by the odd CTA's warp 1)
+  uint64_t* xpeer = epi_bar + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xpeer + (PAIR ? C::kXStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_flag = abort_flag + 1;
   FixJob* fix = reinterpret_cast<FixJob*>(
@@ -383,10 +401,18 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  [[maybe_unused]] const int64_t P = p.num_ctas;   // (index checks)
-  const int64_t cta = blockIdx.x;
-  const int64_t u0 = cta_lo(p, blockIdx.x);
-  const int64_t u1 = cta_lo(p, blockIdx.x + 1);
+  [[maybe_unused]] const int64_t P = p.num_ctas;   // work ranges (index checks)
+  [[maybe_unused]] const int64_t NS = PAIR ? 2 * P : P;   // CTAs: counters, 2 partial slots each
+  // CTA pairs: both CTAs of a cluster share work range cta = blockIdx / 2;
+  // rank 1 takes the odd weight tile and the second half of the activation
+  // rows of every work tile.  Counters and partial slots are per CTA:
+  // sid(c) is this rank's CTA of work range c.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int64_t cta = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  auto sid = [&](int64_t c) -> int64_t { return PAIR ? 2 * c + rank : c; };
+  const int32_t wmul = PAIR ? 2 : 1;   // weight tile of work tile nt: nt * wmul + rank
+  const int64_t u0 = cta_lo(p, static_cast<int32_t>(cta));
+  const int64_t u1 = cta_lo(p, static_cast<int32_t>(cta) + 1);
   const int64_t KS = p.k_units;
   const int32_t ks32 = p.k_units;
   const int32_t tile0_32 = static_cast<int32_t>(u0) / ks32;         // u0 < 2^31
@@ -401,25 +427,38 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       mbar_init(smem_u32(&xfull[i]), 1);
       mbar_init(smem_u32(&mdone[i]), 1);
     }
-    for (int i = 0; i < C::kNumA; ++i) mbar_init(smem_u32(&afull[i]), kDeqGroupWarps);
+    // (CTA pairs: the even CTA's afull and dempty also count the odd CTA's
+    // dequantiser and epilogue warps)
+    for (int i = 0; i < C::kNumA; ++i)
+      mbar_init(smem_u32(&afull[i]), kDeqGroupWarps * (PAIR ? 2 : 1));
     for (int i = 0; i < C::kNumD; ++i) {
       mbar_init(smem_u32(&dfull[i]), C::kMmaThreads);
-      mbar_init(smem_u32(&dempty[i]), 4);
+      mbar_init(smem_u32(&dempty[i]), 4 * (PAIR ? 2 : 1));
     }
     for (int i = 0; i < kMaxMmaThreads; ++i) mbar_init(smem_u32(&fin[i]), 1);
     mbar_init(smem_u32(epi_bar), 4);
+    if constexpr (PAIR)
+      for (int i = 0; i < C::kXStages; ++i) mbar_init(smem_u32(&xpeer[i]), 1);
     *abort_flag = 0;
     *epi_flag = 0;
     fix->valid = 0;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tmap_a);
   tc_fence_before();
-  __syncthreads();
+  // CTA pairs: neither CTA arrives on the other's barriers before both have
+  // initialised them
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   // Programmatic dependent launch.  The next kernel on the stream may begin
@@ -460,14 +499,18 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       // the first ring of weight chunks was issued by an epilogue thread
       // before the grid dependency wait; this stream continues after it
       WeightStream<FMT, BN, KU> ws;
-      ws.init(p, tile0, ku0, ks, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      ws.init(p, tile0, ku0, ks, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages, wmul,
+              static_cast<int32_t>(rank));
       int32_t wi = nu < C::kWStages ? nu : C::kWStages;
       for (int32_t j = 0; j < wi; ++j) ws.advance(p);
       int32_t xi = 0;
       uint32_t xph = 0;
       int32_t x_ku = ku0;
       TileCursor xc = cursor_at<BN>(p, tile0);
-      int32_t xrow = xc.row0 + xc.mt * BN, xk = x_ku * 2 * KU;
+      // first activation row of this CTA's part of the tile (CTA pairs: the
+      // odd CTA holds the second half)
+      const int32_t xhalf = PAIR ? static_cast<int32_t>(rank) * C::kARows : 0;
+      int32_t xrow = xc.row0 + xc.mt * BN + xhalf, xk = x_ku * 2 * KU;
       const uint32_t xdst0 = smem_u32(sm_a);
       const uint32_t wfree0 = smem_u32(&wfree[0]);
       const uint32_t mdone0 = smem_u32(&mdone[0]), xfull0 = smem_u32(&xfull[0]);
@@ -490,7 +533,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         if (xi < nu && mbar_test_wait(mdone0 + xbar, xph ^ 1u)) {
           // the box's first row and slab lie inside A (rows past its end
           // read as zeros) and its destination inside the activation ring
-          if (!PETIT_CHECK(xrow >= 0 && xrow < p.chk_a_rows && xk >= 0 &&
+          if (!PETIT_CHECK(xrow >= 0 && xrow - xhalf < p.chk_a_rows && xk >= 0 &&
                            xk + 2 * KU <= 2 * KU * ks && xdst >= xdst0 &&
                            xdst + C::kABytes <= xdst0 + C::kXStages * C::kABytes &&
                            xbar < 8u * C::kXStages)) {
@@ -513,7 +556,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             x_ku = 0;
             xk = 0;
             cursor_next<BN>(p, xc);
-            xrow = xc.row0 + xc.mt * BN;
+            xrow = xc.row0 + xc.mt * BN + xhalf;
           }
           progress = true;
         }
@@ -540,8 +583,27 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
                             p.timeout_ns, nullptr);
       }
     }
+  } else if (PAIR && warp == kMmaWarp && rank != 0) {
+    // ------------------------------------- activation forwarder (odd CTA)
+    // The even CTA's thread issues the pair's MMAs, which read this CTA's
+    // half of every activation stage: tell it when each half has landed.
+    const int32_t nu = static_cast<int32_t>(u1 - u0);
+    int st = 0;
+    uint32_t ph = 0;
+    for (int32_t i = 0; i < nu; ++i) {
+      if (!PETIT_CHECK(st >= 0 && st < C::kXStages)) break;
+      if (!__all_sync(0xffffffffu, wait(&xfull[st], ph))) break;
+      if (elect_one()) mbar_arrive_remote(mapa_shared(smem_u32(&xpeer[st]), 0));
+      __syncwarp();
+      if (++st == C::kXStages) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
   } else if (warp == kMmaWarp || warp > C::kMmaWarpX) {
     // ------------------------------------------------------------ MMA issue
+    // (CTA pairs: only the even CTA issues; each MMA covers both CTAs'
+    // weight tiles, M = 256, and its completion is signalled to both CTAs)
     const int t = warp == kMmaWarp ? 0 : warp - C::kMmaWarpX;   // issues units i % kMmaThreads == t
     // The whole warp runs the loop, so every operand of tcgen05.mma is
     // warp-uniform and can stay in uniform registers; one elected lane
@@ -551,6 +613,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       auto uwait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, wait(bar, parity));
       };
+
       // Segments (the CTA's units inside one tile) in order; inside a
       // segment only this issuer's units i = t, t + kMmaThreads, ...
       // (CTA-local), whose activation stage, A-buffer and phases advance by
@@ -573,7 +636,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         if (!uwait(&dempty[d], static_cast<uint32_t>(((seg / C::kNumD) & 1) ^ 1))) break;
         bool seg_started = false;   // this issuer has written its accumulator in this segment
         for (; i < s1; i += C::kMmaThreads) {
-          if (!uwait(&xfull[st], ph) || !uwait(&afull[b], pb)) {
+          if (!uwait(&xfull[st], ph) || (PAIR && !uwait(&xpeer[st], ph)) ||
+              !uwait(&afull[b], pb)) {
             ok = false;
             break;
           }
@@ -592,10 +656,19 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
               // K16 step j: slab j / 4 of A, 32-byte offset inside its swizzled rows
               const uint64_t bdesc = smem_desc_kmajor_sw128(a_smem + (j >> 2) * C::kAHalfBytes) +
                                      (((j & 3) * 32) >> 4);
-              mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
-                         (!seg_started && j == 0) ? 0u : 1u);
+              if constexpr (PAIR)
+                mma_ts_f16_pair(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
+                                (!seg_started && j == 0) ? 0u : 1u);
+              else
+                mma_ts_f16(d_tmem, a_tmem + j * 8, bdesc, C::kIdesc,
+                           (!seg_started && j == 0) ? 0u : 1u);
             }
-            mma_commit(smem_u32(&mdone[st]));
+            if constexpr (PAIR) {
+              mma_commit_pair(smem_u32(&mdone[st]));
+              mma_commit_pair(mapa_shared(smem_u32(&mdone[st]), 1));
+            } else {
+              mma_commit(smem_u32(&mdone[st]));
+            }
           }
           __syncwarp();
           seg_started = true;
@@ -612,13 +685,23 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
         }
         if (!ok) break;
         // every issuer arrives once per segment, when its MMAs are done
-        if (elect_one()) mma_commit(smem_u32(&dfull[d]));
+        if (elect_one()) {
+          if constexpr (PAIR) {
+            mma_commit_pair(smem_u32(&dfull[d]));
+            mma_commit_pair(mapa_shared(smem_u32(&dfull[d]), 1));
+          } else {
+            mma_commit(smem_u32(&dfull[d]));
+          }
+        }
         __syncwarp();
         ++seg;
         s0 = s1;
       }
       // all issued MMAs complete before tensor memory is released
-      if (elect_one()) mma_commit(smem_u32(&fin[t]));
+      if (elect_one()) {
+        if constexpr (PAIR) mma_commit_pair(smem_u32(&fin[t]));
+        else mma_commit(smem_u32(&fin[t]));
+      }
       __syncwarp();
       mbar_wait_bounded(smem_u32(&fin[t]), 0, p.timeout_ns, nullptr);
     }
@@ -635,7 +718,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       // this idle thread does it and the producer reaches the dependency
       // wait, and the activation copies after it, without delay.
       WeightStream<FMT, BN, KU> ws;
-      ws.init(p, tile0_32, ku0_32, ks32, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages);
+      ws.init(p, tile0_32, ku0_32, ks32, smem_u32(sm_w), smem_u32(&wfull[0]), C::kWStages, wmul,
+              static_cast<int32_t>(rank));
       const uint64_t policy = p.weights_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
       for (int64_t j = 0; j < u1 - u0 && j < C::kWStages; ++j) {
         if (PETIT_CHECK(ws.in_bounds(p))) ws.issue(p, policy);
@@ -646,11 +730,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       // first ring of weight chunks of its partner in the upper half into
       // L2, so that partner's first copies hit L2.
       const int32_t half = (p.num_ctas + 1) / 2;
-      if (blockIdx.x + half < p.num_ctas) {
-        const int32_t pc = blockIdx.x + half;
+      if (cta + half < p.num_ctas) {
+        const int32_t pc = static_cast<int32_t>(cta) + half;
         const int32_t pu0 = cta_lo(p, pc), pn = cta_lo(p, pc + 1) - pu0;
         WeightStream<FMT, BN, KU> pw;
-        pw.init(p, pu0 / ks32, pu0 % ks32, ks32, 0, 0, C::kWStages);
+        pw.init(p, pu0 / ks32, pu0 % ks32, ks32, 0, 0, C::kWStages, wmul,
+                static_cast<int32_t>(rank));
         for (int32_t j = 0; j < pn && j < C::kWStages; ++j) {
           if (!PETIT_CHECK(pw.in_bounds(p))) break;
           bulk_prefetch_l2(pw.src, WeightStream<FMT, BN, KU>::kBytes);
@@ -695,11 +780,12 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       if (!full_tile) {
         c_first = cta_of_unit(p, tile * KS);
         c_last = cta_of_unit(p, (tile + 1) * KS - 1);
-        first_slot = 2 * c_first + (cta_lo(p, static_cast<int32_t>(c_first)) / KS == tile ? 0 : 1);
-        if (!PETIT_CHECK(c_first >= 0 && c_first <= c_last && c_last < P && c_first < kMaxCtas &&
-                         first_slot >= 0 && first_slot < 2 * P))
+        first_slot =
+            2 * sid(c_first) + (cta_lo(p, static_cast<int32_t>(c_first)) / KS == tile ? 0 : 1);
+        if (!PETIT_CHECK(c_first >= 0 && c_first <= c_last && c_last < P &&
+                         sid(c_first) < kMaxCtas && first_slot >= 0 && first_slot < 2 * NS))
           break;
-        ctr = &p.counters[c_first];
+        ctr = &p.counters[sid(c_first)];
         // first look while the segment's MMAs run
         if (last_seg && epi_tid == 0)
           *epi_flag = ld_acquire_gpu(ctr) == static_cast<uint32_t>(c_last - c_first);
@@ -731,7 +817,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             fix->c_last = c_last;
             fix->first_slot = first_slot;
             fix->row0 = static_cast<int64_t>(mt) * BN;
-            fix->col0 = static_cast<int64_t>(nt) * kTileN;
+            fix->col0 = (static_cast<int64_t>(nt) * wmul + rank) * kTileN;
             fix->g_rows = g_rows;
             fix->alpha = alpha;
             fix->d = d;
@@ -744,11 +830,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       }
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase + d * BN;
-      const int64_t ncol = static_cast<int64_t>(nt) * kTileN + r;
-      const int64_t slot = 2 * cta + (tile == first_tile_of_cta ? 0 : 1);
+      const int64_t ncol = (static_cast<int64_t>(nt) * wmul + rank) * kTileN + r;
+      const int64_t slot = 2 * sid(cta) + (tile == first_tile_of_cta ? 0 : 1);
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
       // (a partial slot holds BN x 128 floats; r < 128)
-      if (!full_tile && !PETIT_CHECK(slot >= 0 && slot < 2 * P)) break;
+      if (!full_tile && !PETIT_CHECK(slot >= 0 && slot < 2 * NS)) break;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         // the contributing accumulators, added in issuer order
@@ -781,7 +867,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&dempty[d]));
+      if (lane == 0) {
+        // (CTA pairs: the even CTA's issuer waits for both CTAs' epilogues)
+        if (PAIR && rank != 0) mbar_arrive_remote(mapa_shared(smem_u32(&dempty[d]), 0));
+        else mbar_arrive(smem_u32(&dempty[d]));
+      }
       if (!full_tile) {
         // Ordering without per-thread fences: the group barrier (mbarrier
         // arrive = release, wait = acquire, CTA scope) orders every epilogue
@@ -805,7 +895,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             fix->c_last = c_last;
             fix->first_slot = first_slot;
             fix->row0 = static_cast<int64_t>(mt) * BN;
-            fix->col0 = static_cast<int64_t>(nt) * kTileN;
+            fix->col0 = (static_cast<int64_t>(nt) * wmul + rank) * kTileN;
             fix->g_rows = g_rows;
             fix->alpha = alpha;
             fix->d = d;
@@ -828,8 +918,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
               for (int x = 0; x < kFixBatch; ++x) {
                 const int64_t c = cb + x;
                 if (c <= c_last) {
-                  const int64_t cs = c == c_first ? first_slot : 2 * c;
-                  if (!PETIT_CHECK(cs >= 0 && cs < 2 * P)) continue;
+                  const int64_t cs = c == c_first ? first_slot : 2 * sid(c);
+                  if (!PETIT_CHECK(cs >= 0 && cs < 2 * NS)) continue;
                   const float* src =
                       p.partials + static_cast<size_t>(cs) * (BN * kTileN) + c0 * kTileN + r;
 #pragma unroll
@@ -935,7 +1025,11 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
+      if (lane == 0) {
+        // (CTA pairs: the even CTA's MMA reads both CTAs' A-buffers)
+        if (PAIR && rank != 0) mbar_arrive_remote(mapa_shared(smem_u32(&afull[b]), 0));
+        else mbar_arrive(smem_u32(&afull[b]));
+      }
       st += G;
       if (st >= C::kWStages) {
         st -= C::kWStages;
@@ -973,7 +1067,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     const int fg = warp >> 2;
     if (fg < kFixGroups && !*abort_flag &&
         PETIT_CHECK(f.d >= 0 && f.d < C::kNumD && f.c_first >= 0 && f.c_first <= cta &&
-                    cta <= f.c_last && f.c_last < P && f.first_slot >= 0 && f.first_slot < 2 * P)) {
+                    cta <= f.c_last && f.c_last < P && f.first_slot >= 0 &&
+                    f.first_slot < 2 * NS)) {
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase +
@@ -1011,7 +1106,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
             const int64_t c = cb + x;
             if (c <= f.c_last && c != cta) {
               const float* src = p.partials +
-                                 static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * c) *
+                                 static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * sid(c)) *
                                      (BN * kTileN) +
                                  m0 * kTileN + r;
 #pragma unroll
@@ -1041,42 +1136,98 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU>::kThreads), 1)
     __syncthreads();
     tc_fence_after();
   }
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if constexpr (PAIR) {
+    // Neither CTA of a pair frees its tensor memory or exits while the
+    // other may still use it: the even CTA's MMAs (all complete once its
+    // issuer's final commit has been waited on) read and write both CTAs'
+    // tensor memory and read the odd CTA's shared memory, and each CTA
+    // arrives on the other's barriers.  Every thread of both CTAs gets here
+    // after bounded work only.
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc_pair(tmem, kTmemCols);
+  } else {
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  }
   // a wait that ran out anywhere in the CTA is reported by thread 0, which
   // has passed the grid dependency wait
   if (threadIdx.x == 0 && *abort_flag)
     atomicOr(p.status, (*abort_flag & kAbortBounds) ? kStatusBounds : kStatusTimeout);
 }
 
-template <int FMT, int BN, int KU>
+template <int FMT, int BN, int KU, bool PAIR = false>
 cudaError_t launch_t(const Params& prm, const CUtensorMap& tmap, cudaStream_t stream, int dev) {
-  using C = Cfg<FMT, BN, KU>;
+  using C = Cfg<FMT, BN, KU, PAIR>;
   // the dynamic shared-memory limit is raised once per device
   static std::atomic<bool> attr_done[64];
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, KU>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, KU, PAIR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(prm.num_ctas));
+  // CTA pairs: two CTAs (a cluster) per work range
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.num_ctas * (PAIR ? 2 : 1)));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN, KU, PAIR>, prm, tmap);
+}
+
+// How many CTA pairs of the pair kernel (this format and tile height) can be
+// resident at once on the current device; 0 if the query fails.
+template <int FMT, int BN>
+int pair_capacity_t() {
+  using C = Cfg<FMT, BN, 1, true>;
+  auto kern = gemm_kernel<FMT, BN, 1, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * kMaxBoundCtas);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN, KU>, prm, tmap);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 template <int FMT>
-cudaError_t launch_fmt(int bn, int ku, const Params& prm, const CUtensorMap& tmap, cudaStream_t s,
-                       int dev) {
+cudaError_t launch_fmt(int bn, int ku, bool pair, const Params& prm, const CUtensorMap& tmap,
+                       cudaStream_t s, int dev) {
+  if (pair) {
+    if (ku != 1) return cudaErrorInvalidValue;
+    switch (bn) {
+      case 128: return launch_t<FMT, 128, 1, true>(prm, tmap, s, dev);
+      case 256: return launch_t<FMT, 256, 1, true>(prm, tmap, s, dev);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (ku == 2) {
     switch (bn) {
       case 16: return launch_t<FMT, 16, 2>(prm, tmap, s, dev);
@@ -1143,6 +1294,7 @@ void plan_bounds(GemmPlan& pl, double late_ns) {
 }
 
 std::atomic<int> g_tile_override{0};   // bn | ku << 16, or 0: the planner decides
+std::atomic<int> g_pair_mode{0};       // 0: CTA pairs where they pay, 1: never, 2: wherever possible
 // bounds-checking build: extents the checks use in place of the true ones
 // (negative: the true extent)
 std::atomic<int64_t> g_check_weight_bytes{-1};
@@ -1153,6 +1305,21 @@ double late_start_ns() { return kLateStartNs; }
 }  // namespace
 
 int tile_override() { return g_tile_override.load(std::memory_order_relaxed); }
+
+bool set_pair_mode(int mode) {
+  if (mode < 0 || mode > 2) return false;
+  g_pair_mode.store(mode);
+  return true;
+}
+
+int pair_capacity() {
+  int cap = 1 << 30;
+  for (const int c : {pair_capacity_t<kNVFP4, 128>(), pair_capacity_t<kNVFP4, 256>(),
+                      pair_capacity_t<kMXFP4, 128>(), pair_capacity_t<kMXFP4, 256>(),
+                      pair_capacity_t<kNVFP4F16, 128>(), pair_capacity_t<kNVFP4F16, 256>()})
+    cap = std::min(cap, c);
+  return std::min(cap, kMaxBoundCtas);
+}
 
 bool bounds_checking() {
 #ifdef PETIT_CHECK_BOUNDS
@@ -1182,7 +1349,7 @@ bool set_tile_override(int bn, int ku) {
 }
 
 GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
-                      int num_sms) {
+                      int num_sms, int pair_cap) {
   GemmPlan pl{};
   pl.fmt = fmt;
   pl.num_groups = num_groups;
@@ -1208,7 +1375,12 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
         pl.bn = bn;
       }
     }
-  } else if (pl.bn == 256 && m <= 256) {
+  }
+  // CTA pairs (cta_group::2 MMAs over two adjacent weight tiles) for 128-
+  // and 256-row tiles of a single GEMM whose n holds whole tile pairs
+  const int pair_mode = g_pair_mode.load(std::memory_order_relaxed);
+  const bool pair_ok = pair_cap > 0 && num_groups == 1 && n % (2 * kTileN) == 0 && pair_mode != 1;
+  if (num_groups == 1 && pl.bn == 256 && m <= 256) {
     // N = 256 dequantises each weight once for all rows, but halves the
     // number of work units; small matrices keep two 128-row tiles so that
     // every CTA still has a long pipeline to amortise its fixed costs over
@@ -1224,7 +1396,17 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
     pl.bn = ov & 0xFFFF;
     pl.ku = ((ov >> 16) == 2 && pl.bn <= 64 && (k / kStageK) % 2 == 0) ? 2 : 1;
   }
-  pl.n_tiles = static_cast<int>(n / kTileN);
+  // Measured on GB300 (Llama-3-70B shapes, m = 128..512): CTA pairs are
+  // 5-14 % faster with 256-row tiles and on large matrices with 128-row
+  // tiles (gate_up), and level with single CTAs on small 128-row-tile
+  // problems (QKV, O: 27-67 pair units per range), which stay on single CTAs
+  if (pair_ok && pl.bn >= 128 && pl.ku == 1) {
+    const int64_t pair_units = static_cast<int64_t>(n / (2 * kTileN)) * (k / kStageK) *
+                               ((m + pl.bn - 1) / pl.bn);
+    pl.pair = pair_mode == 2 || pl.bn == 256 || pair_units >= 100 * static_cast<int64_t>(pair_cap);
+  }
+  // work tiles: 128 weight rows, or 256 (a tile pair) with CTA pairs
+  pl.n_tiles = static_cast<int>(n / (kTileN * (pl.pair ? 2 : 1)));
   pl.k_stages = static_cast<int>(k / kStageK);
   int64_t tiles = 0;
   for (int g = 0; g <= num_groups; ++g) {
@@ -1236,20 +1418,23 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
     tiles += mt * pl.n_tiles;
   }
   pl.units = tiles * (pl.k_stages / pl.ku);
-  pl.num_ctas = static_cast<int>(pl.units < num_sms ? pl.units : num_sms);
+  // work ranges: one per SM, or one per resident CTA pair
+  const int64_t ranges = pl.pair ? pair_cap : num_sms;
+  pl.num_ctas = static_cast<int>(pl.units < ranges ? pl.units : ranges);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
-  if (pl.num_ctas > kMaxCtas) pl.num_ctas = kMaxCtas;
+  if (pl.num_ctas * (pl.pair ? 2 : 1) > kMaxCtas) pl.num_ctas = kMaxCtas / (pl.pair ? 2 : 1);
   if (pl.units < (int64_t(1) << 31)) plan_bounds(pl, late_start_ns());
   pl.ws.counters_off = kWsHeaderBytes;
   pl.ws.partials_off = align_up(kWsHeaderBytes + kWsCountersBytes, 256);
-  pl.ws.total = pl.ws.partials_off +
-                sizeof(float) * 2ull * static_cast<size_t>(pl.num_ctas) * pl.bn * kTileN;
+  // two partial slots per CTA (a work range has two CTAs with CTA pairs)
+  pl.ws.total = pl.ws.partials_off + sizeof(float) * 2ull * static_cast<size_t>(pl.num_ctas) *
+                                         (pl.pair ? 2 : 1) * pl.bn * kTileN;
   return pl;
 }
 
-GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms) {
+GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms, int pair_cap) {
   const int64_t off[2] = {0, m};
-  return plan_grouped(off, 1, n, k, fmt, num_sms);
+  return plan_grouped(off, 1, n, k, fmt, num_sms, pair_cap);
 }
 
 cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap& tmap,
@@ -1286,7 +1471,8 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
   {
     const int64_t chunk = pl.fmt == kMXFP4 ? FmtTraits<kMXFP4>::kChunkBytes
                                            : FmtTraits<kNVFP4>::kChunkBytes;
-    const int64_t wb = static_cast<int64_t>(pl.n_tiles) * pl.k_stages * chunk;
+    // (with CTA pairs a work tile holds two 128-row weight tiles)
+    const int64_t wb = static_cast<int64_t>(pl.n_tiles) * (pl.pair ? 2 : 1) * pl.k_stages * chunk;
     const int64_t ce = static_cast<int64_t>(pl.row_off[pl.num_groups]) * a.n;
     const int64_t lw = g_check_weight_bytes.load(), lc = g_check_c_elems.load();
     prm.chk_rep_bytes = lw >= 0 && lw < wb ? lw : wb;
@@ -1294,9 +1480,11 @@ cudaError_t launch_gemm(const GemmPlan& pl, const GemmArgs& a, const CUtensorMap
     prm.chk_a_rows = pl.row_off[pl.num_groups];
   }
 #endif
-  if (pl.fmt == kNVFP4) return launch_fmt<kNVFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);
-  if (pl.fmt == kNVFP4F16) return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, prm, tmap, stream, a.device);
-  return launch_fmt<kMXFP4>(pl.bn, pl.ku, prm, tmap, stream, a.device);
+  if (pl.fmt == kNVFP4)
+    return launch_fmt<kNVFP4>(pl.bn, pl.ku, pl.pair, prm, tmap, stream, a.device);
+  if (pl.fmt == kNVFP4F16)
+    return launch_fmt<kNVFP4F16>(pl.bn, pl.ku, pl.pair, prm, tmap, stream, a.device);
+  return launch_fmt<kMXFP4>(pl.bn, pl.ku, pl.pair, prm, tmap, stream, a.device);
 }
 
 }  // namespace petit

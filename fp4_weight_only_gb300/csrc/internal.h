@@ -41,10 +41,14 @@ struct GemmPlan {
   int fmt;
   int bn;          // activation rows per tile (MMA N)
   int ku;          // 128-k chunks per pipeline unit (1 or 2)
-  int n_tiles;
+  // CTA pairs: two CTAs of a cluster per work range, on a pair of adjacent
+  // 128-row weight tiles (cta_group::2 MMAs); work tiles are then 256
+  // weight rows and num_ctas counts work ranges (pairs)
+  bool pair;
+  int n_tiles;     // work tiles along n
   int k_stages;    // 128-k chunks per tile row
   int64_t units;   // tiles * k_stages / ku
-  int num_ctas;
+  int num_ctas;    // work ranges (CTAs, or CTA pairs)
   // stream-K ranges: CTA c covers units [bound[c], bound[c+1]) when
   // use_bounds, else an even split
   bool use_bounds;
@@ -56,7 +60,9 @@ struct GemmPlan {
   WsLayout ws;
 };
 
-GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms);
+// pair_cap: CTA pairs that can be resident at once (pair_capacity()), 0 to
+// plan without CTA pairs
+GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms, int pair_cap);
 // Process-wide forced tile shape for the planner (tuning and tests): bn in
 // {16, 32, 64, 128, 256}, ku in {1, 2} (2 only for bn <= 64); (0, 0) clears.
 // Returns false for any other pair.
@@ -70,7 +76,12 @@ bool bounds_checking();
 bool set_check_limits(int64_t weight_bytes, int64_t c_elems);
 // row_off: num_groups + 1 non-decreasing offsets starting at 0
 GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t k, int fmt,
-                      int num_sms);
+                      int num_sms, int pair_cap);
+// Resident CTA pairs of the pair kernels on the current device (0 if none).
+int pair_capacity();
+// 0: CTA pairs where the planner expects them to pay, 1: never, 2: wherever
+// they apply (tests and tuning).  Returns false for any other value.
+bool set_pair_mode(int mode);
 
 struct GemmArgs {
   const void* A;

@@ -305,6 +305,20 @@ petit_status_t petit_gemm_bf16_nvfp4_noalloc(const void* A, const uint8_t* rep,
  * other host threads.  Errors: PETIT_ERR_INVALID_ARG for any other pair. */
 petit_status_t petit_set_tile_config(int bn, int ku);
 
+/* CTA pairs for 128- and 256-row activation tiles.  A single GEMM whose n is
+ * a multiple of 256 can run on clusters of two CTAs that take adjacent
+ * 128-row weight tiles of the same 256-row work tile; one thread of the pair
+ * issues tcgen05 MMAs of M = 256 (cta_group::2) that read both CTAs'
+ * dequantised weights, and each CTA holds half of the tile's activation
+ * rows, so each SM moves half the activation bytes.  Mode 0 (the default)
+ * uses them where the planner expects a gain (256-row tiles, and 128-row
+ * tiles of large matrices), mode 1 never, mode 2 wherever they apply (tests
+ * and tuning).  Results differ between modes in FP32 summation order only.
+ * Not thread-safe with respect to GEMM calls running concurrently on other
+ * host threads; query workspace sizes after the call.  Errors:
+ * PETIT_ERR_INVALID_ARG for any other mode. */
+petit_status_t petit_set_pair_mode(int mode);
+
 /* ------------------------------------------------- bounds-checking build */
 
 /* The library also builds as _petit_check.so with every global-memory

@@ -96,6 +96,14 @@ def test_no_device_is_reported_not_crashed(lib):
     assert lib.petit_gemm_workspace_bytes(16, 1024, 1024, 0) == 0
 
 
+def test_pair_mode_validation(lib):
+    for mode in (0, 1, 2):
+        assert lib.petit_set_pair_mode(mode) == 0
+    assert lib.petit_set_pair_mode(3) == 1
+    assert lib.petit_set_pair_mode(-1) == 1
+    assert lib.petit_set_pair_mode(0) == 0
+
+
 def test_tile_config_override_validation(lib):
     assert lib.petit_set_tile_config(48, 1) == 1
     assert lib.petit_set_tile_config(128, 2) == 1

@@ -8,8 +8,9 @@ are the failure the CUTLASS FP4 article describes (sections 5.1 and 7); this
 build turns them into a status.
 
 * Every kernel shape (tile heights 16..256, one or two chunks per unit,
-  split tiles, ragged m), both formats, the FP16 layout, the grouped MoE
-  launch and the no-allocation entry point run with all checks passing:
+  split tiles, ragged m), the CTA-pair kernel, both formats, the FP16
+  layout, the grouped MoE launch and the no-allocation entry point run with
+  all checks passing:
   status OK and results within the oracle tolerances.
 * A check is made to fail without any access leaving its real buffer: the
   extents the checks use are lowered (weights, then C) below the true ones.
@@ -64,6 +65,27 @@ def test_every_tile_shape_passes_its_checks(chk, bn, ku):
         chk.set_tile_config(0, 0)
     assert ws.status() == OK
     assert_parity(c, oracle_reference(a, codes, scales, "nvfp4"), f"bn={bn} ku={ku}")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("m", [40, 200])
+def test_cta_pairs_pass_their_checks(chk, bn, m):
+    """The CTA-pair kernel (forced), including a tile whose second half of
+    activation rows lies entirely past m."""
+    n, k = 1024, 2048
+    w = synth.weights(n, k, seed=bn + m)
+    codes, scales, rep = _prep(chk, w, "mxfp4")
+    a = synth.activations(m, k, seed=m)
+    ws = chk.Workspace()
+    chk.set_pair_mode(2)
+    chk.set_tile_config(bn, 1)
+    try:
+        c = chk.gemm(a.cuda(), rep, n, "mxfp4", 1.0, workspace=ws)
+    finally:
+        chk.set_tile_config(0, 0)
+        chk.set_pair_mode(0)
+    assert ws.status() == OK
+    assert_parity(c, oracle_reference(a, codes, scales, "mxfp4"), f"pairs bn={bn} m={m}")
 
 
 @pytest.mark.parametrize("fmt,m,k", [("nvfp4", 16, 4096), ("nvfp4", 5, 3968), ("mxfp4", 16, 4096),
