@@ -261,12 +261,16 @@ struct Cfg {
   static constexpr int kABytes = 2 * KU * kAHalfBytes;
   static constexpr int kWBytes = KU * T::kChunkBytes;          // codes + scales
   // MMA-issuing threads.  A thread issues one tcgen05.mma per ~65 cycles
-  // whatever N is, so short (N <= 128) MMAs need several issuers on
+  // whatever N is, so short (N <= 32) MMAs need several issuers on
   // different SM sub-partitions.  They take the CTA's units round-robin,
   // each into its own accumulator, which the epilogue adds in a fixed order.
   // Three issuers (warps 1, 14, 15 on sub-partitions 1, 2, 3) keep the CTA
   // at 16 warps, four per sub-partition, so each thread may use 128 registers.
-  static constexpr int kMmaThreads = PAIR ? 1 : BN <= 32 ? 3 : BN <= 128 ? 2 : 1;
+  // At N = 64 one issuer leaves room for two accumulators, so a tile's
+  // epilogue overlaps the next tile's MMAs (measured on GB300: gate_up at
+  // m = 64 12 % faster than with two issuers and one accumulator each); at
+  // N = 128 two issuers stay faster.
+  static constexpr int kMmaThreads = PAIR ? 1 : BN <= 32 ? 3 : BN == 128 ? 2 : 1;
   // dequantiser groups (four warps each) taking units round-robin
   static constexpr int kDeqGroups = 2;
   static constexpr int kMmaWarpX = kDeqWarp0 + kDeqGroupWarps * kDeqGroups - 1;  // issuer t>=1: +t
@@ -1423,6 +1427,30 @@ GemmPlan plan_grouped(const int64_t* row_off, int num_groups, int64_t n, int64_t
   pl.num_ctas = static_cast<int>(pl.units < ranges ? pl.units : ranges);
   if (pl.num_ctas < 1) pl.num_ctas = 1;
   if (pl.num_ctas * (pl.pair ? 2 : 1) > kMaxCtas) pl.num_ctas = kMaxCtas / (pl.pair ? 2 : 1);
+  if (!pl.pair && pl.bn == 128 && num_groups == 1) {
+    // Tile-aligned ranges.  With 128-row tiles each of the two MMA issuers
+    // has one accumulator, so a range that crosses a tile boundary stalls
+    // its MMAs while the epilogue drains the finished tile: measured on
+    // GB300 at about 15 units' time.  Where whole tiles, or equal parts of
+    // them, give every CTA one segment on fewer CTAs for less total time,
+    // take that (O at m = 128: 26.0 -> 23.7 us, at m = 256: 36.5 -> 35.0 us
+    // on 128 CTAs; QKV, and down with its long tiles, keep every SM).
+    const int64_t per_tile = pl.k_stages / pl.ku;
+    auto cost = [&](int64_t P, bool aligned) {
+      const double L = static_cast<double>((pl.units + P - 1) / P);
+      return L + (aligned ? 0.0 : 15.0 * static_cast<double>(pl.units) / P / per_tile);
+    };
+    double best = cost(pl.num_ctas, false);
+    for (int64_t parts = 1; parts <= 4; ++parts) {
+      const int64_t P = tiles * parts;
+      if (P > num_sms || per_tile % parts != 0) continue;
+      const double c = cost(P, true);
+      if (c < best) {
+        best = c;
+        pl.num_ctas = static_cast<int>(P);
+      }
+    }
+  }
   if (pl.units < (int64_t(1) << 31)) plan_bounds(pl, late_start_ns());
   pl.ws.counters_off = kWsHeaderBytes;
   pl.ws.partials_off = align_up(kWsHeaderBytes + kWsCountersBytes, 256);
