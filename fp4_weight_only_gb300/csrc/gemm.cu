@@ -45,6 +45,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -981,49 +982,86 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
         break;
       if (!wait(&wfull[st], ph)) break;
       bool ok = true;
+      if constexpr (FMT == kMXFP4) {
+        // The repack's per-chunk flag bytes (warp-uniform), read once per
+        // unit: the unit's decode takes one multiply per word when every
+        // scale code of its chunks is <= 128 (both variants of the loop are
+        // compiled; a flag test inside the unrolled loop cost 5 % of the
+        // MXFP4 decode step).
+        bool fast = true;
 #pragma unroll
-      for (int hj = 0; hj < 2 * KU; ++hj) {
-        const int h = hj / KU, j = hj % KU;
-        const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
-        const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
-        const uint4 g1 = *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
-        uint32_t o[2][16];
-        if constexpr (FMT == kNVFP4 || FMT == kNVFP4F16) {
+        for (int j = 0; j < KU; ++j)
+          fast = fast &&
+                 sm_w[st * C::kWBytes + j * T::kChunkBytes + kWChunkBytes + T::kSChunkBytes];
+        auto unit = [&](auto fast_tag) {
+          constexpr bool kFast = decltype(fast_tag)::value;
+#pragma unroll
+          for (int hj = 0; hj < 2 * KU; ++hj) {
+            const int h = hj / KU, j = hj % KU;
+            const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+            const uint4 g0 =
+                *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+            const uint4 g1 =
+                *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+            uint32_t o[2][16];
+            const uint32_t sv =
+                *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
+            decode_group<FMT, kFast>(g0, sv & 0xFFu, o[0]);
+            decode_group<FMT, kFast>(g1, (sv >> 8) & 0xFFu, o[1]);
+            if (hj == 2 * KU - 1) {
+              // the decode consumed every byte this warp read: release the chunk
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
+            }
+            if (hj == 0 && i >= C::kNumA) {
+              // A-buffer b was last used by unit i - kNumA: wait for its
+              // MMAs, and order the stores below after their operand reads
+              if (!wait(&mdone[st2], ph2)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t acol =
+                tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+            tmem_st_x16(acol, o[0]);
+            tmem_st_x16(acol + 16, o[1]);
+          }
+        };
+        if (fast) unit(std::true_type{});
+        else unit(std::false_type{});
+      } else {
+#pragma unroll
+        for (int hj = 0; hj < 2 * KU; ++hj) {
+          const int h = hj / KU, j = hj % KU;
+          const uint8_t* chunk = sm_w + st * C::kWBytes + j * T::kChunkBytes;
+          const uint4 g0 = *reinterpret_cast<const uint4*>(chunk + ((2 * h) * kTileN + r) * 16);
+          const uint4 g1 =
+              *reinterpret_cast<const uint4*>(chunk + ((2 * h + 1) * kTileN + r) * 16);
+          uint32_t o[2][16];
           const uint32_t sv =
               *reinterpret_cast<const uint32_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 4);
           decode_group<FMT>(g0, sv & 0xFFFFu, o[0]);
           decode_group<FMT>(g1, sv >> 16, o[1]);
-        } else {
-          const uint32_t sv =
-              *reinterpret_cast<const uint16_t*>(chunk + kWChunkBytes + (h * kTileN + r) * 2);
-          // the repack's per-chunk flag (warp-uniform): one multiply per
-          // word when every scale code of the chunk is <= 128
-          if (chunk[kWChunkBytes + T::kSChunkBytes]) {
-            decode_group<FMT, true>(g0, sv & 0xFFu, o[0]);
-            decode_group<FMT, true>(g1, sv >> 8, o[1]);
-          } else {
-            decode_group<FMT>(g0, sv & 0xFFu, o[0]);
-            decode_group<FMT>(g1, (sv >> 8) & 0xFFu, o[1]);
+          if (hj == 2 * KU - 1) {
+            // the decode consumed every byte this warp read: release the chunk
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
           }
-        }
-        if (hj == 2 * KU - 1) {
-          // the decode consumed every byte this warp read: release the chunk
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&wfree[st]));
-        }
-        if (hj == 0 && i >= C::kNumA) {
-          // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
-          // and order the stores below after their operand reads
-          if (!wait(&mdone[st2], ph2)) {
-            ok = false;
-            break;
+          if (hj == 0 && i >= C::kNumA) {
+            // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
+            // and order the stores below after their operand reads
+            if (!wait(&mdone[st2], ph2)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
+          const uint32_t acol =
+              tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
+          tmem_st_x16(acol, o[0]);
+          tmem_st_x16(acol + 16, o[1]);
         }
-        const uint32_t acol =
-            tmem + lane_base + b * C::kAColsPerUnit + j * (kStageK / 2) + (2 * h) * 16;
-        tmem_st_x16(acol, o[0]);
-        tmem_st_x16(acol + 16, o[1]);
       }
       if (!ok) break;
       tmem_wait_st();
