@@ -310,7 +310,11 @@ struct Cfg {
   static constexpr int kNumA1 = (kNumA0 > 4 ? 4 : kNumA0) / kMmaThreads * kMmaThreads;
   static constexpr int kNumA = kNumA1 > kXStages ? kXStages / kMmaThreads * kMmaThreads : kNumA1;
   static constexpr int kDColBase = kNumA * kAColsPerUnit;      // D(t, d) at + (t*kNumD+d)*BN
-  static constexpr int kSmemBytes = 1024 + kXStages * kABytes + kWStages * kWBytes + 1024;
+  // 128/256-row tiles: 16 output rows x 128 columns of BF16 staged in
+  // shared memory, so that C is written in whole 256-byte row segments
+  static constexpr int kStageC = BN >= 128 ? 16 * kTileN * 2 : 0;
+  static constexpr int kSmemBytes =
+      1024 + kXStages * kABytes + kWStages * kWBytes + 1024 + kStageC;
   static constexpr uint32_t kM = PAIR ? 256 : 128;   // MMA M (weight rows of both CTAs)
   static constexpr uint32_t kIdesc =
       FMT == kNVFP4F16 ? idesc_f16_f32(kM, BN) : idesc_bf16_f32(kM, BN);
@@ -403,6 +407,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
   volatile int* epi_flag = abort_flag + 1;
   FixJob* fix = reinterpret_cast<FixJob*>(
       (reinterpret_cast<uintptr_t>(epi_flag + 1) + 15) & ~static_cast<uintptr_t>(15));
+  // output staging (kStageC bytes) after the 1024-byte barrier region
+  uint16_t* stage_c = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -765,6 +771,34 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
       ++epi_phase;
       return ok;
     };
+    // 128/256-row tiles: 16 rows (row0 .. row0 + 15 of group g's output,
+    // columns col0 + 0..127) from the four epilogue warps, each holding its
+    // 32 columns, are staged in shared memory and written as whole 256-byte
+    // row segments, a 16-byte vector per lane.  Stored directly, each warp's
+    // 64-byte piece of each row took ~5x as long (measured on GB300: 10 us
+    // against 2 us to drain a 256-row tile of the gate_up projection).
+    auto put_rows = [&](const float (&val)[16], uint16_t* c_g, int64_t row0, int64_t col0,
+                        int64_t g_rows, float alpha) {
+      if constexpr (C::kStageC > 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stage_c[j * kTileN + r] = out_bits<FMT>(alpha * val[j]);
+        if (!epi_sync()) return false;
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int row = 4 * q + 2 * s2 + (lane >> 4);   // warp q writes rows 4q .. 4q + 3
+          const int col = (lane & 15) * 8;
+          const int64_t mrow = row0 + row;
+          if (mrow < g_rows &&
+              PETIT_CHECK(col0 + col + 8 <= p.n &&
+                          (c_g - p.c) + mrow * p.n + col0 + col + 8 <= p.chk_c_elems))
+            *reinterpret_cast<uint4*>(c_g + mrow * p.n + col0 + col) =
+                *reinterpret_cast<const uint4*>(stage_c + row * kTileN + col);
+        }
+        return epi_sync();   // before the buffer is written again
+      } else {
+        return false;
+      }
+    };
     for (int64_t u = u0; u < u1; ++seg) {
       const int64_t tile = u / KS;
       const int64_t seg_end = (tile + 1) * KS < u1 ? (tile + 1) * KS : u1;
@@ -840,6 +874,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
       float* my_slot = p.partials + static_cast<size_t>(slot) * (BN * kTileN);
       // (a partial slot holds BN x 128 floats; r < 128)
       if (!full_tile && !PETIT_CHECK(slot >= 0 && slot < 2 * NS)) break;
+      bool c_ok = true;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         // the contributing accumulators, added in issuer order
@@ -857,7 +892,15 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
             have = true;
           }
         }
-        if (full_tile) {
+        if (full_tile && C::kStageC > 0) {
+          float fv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) fv[j] = __uint_as_float(v[j]);
+          if (!put_rows(fv, c_g, static_cast<int64_t>(mt) * BN + c0, ncol - r, g_rows, alpha)) {
+            c_ok = false;
+            break;
+          }
+        } else if (full_tile) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
@@ -870,6 +913,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
           for (int j = 0; j < 16; ++j) my_slot[(c0 + j) * kTileN + r] = __uint_as_float(v[j]);
         }
       }
+      if (!c_ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -939,6 +983,8 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
                 }
               }
             }
+            // (stored directly: here the partial loads set the pace, and
+            // staging, with its barriers between the warps, was slower)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int64_t mrow = static_cast<int64_t>(mt) * BN + c0 + j;
