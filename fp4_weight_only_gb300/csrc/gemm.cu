@@ -1147,82 +1147,177 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
   // at consecutive addresses), adds them in CTA order and writes C.  The
   // epilogue's acquire of the arrival counter reaches every thread through
   // the barrier above.
-  if (fix->valid && !*abort_flag) {
-    const FixJob f = *fix;
-    constexpr int kFixGroups = C::kThreads / 32 >= 16 ? 4 : 2;
-    constexpr int kCols = BN / kFixGroups;               // activation rows per group
-    constexpr int kLd = kCols >= 16 ? 16 : 4;            // columns per tensor-memory load
-    const int fg = warp >> 2;
-    if (fg < kFixGroups && !*abort_flag &&
-        PETIT_CHECK(f.d >= 0 && f.d < C::kNumD && f.c_first >= 0 && f.c_first <= cta &&
-                    cta <= f.c_last && f.c_last < P && f.first_slot >= 0 &&
-                    f.first_slot < 2 * NS)) {
+  if constexpr (C::kStageC > 0) {
+    // 128/256-row tiles: the same sum, written through a shared-memory stage
+    // in 256-byte row segments (as the epilogue writes whole tiles); the
+    // activation ring is free by now and holds one 16-row stage per group.
+    // Every warp runs the same loop, so the CTA-wide barriers match; the
+    // decision to run it is read by all threads before any check below can
+    // raise the abort flag.
+    const bool run_fix = fix->valid && !*abort_flag;
+    __syncthreads();
+    if (run_fix) {
+      const FixJob f = *fix;
+      constexpr int kFixGroups = C::kThreads / 32 >= 16 ? 4 : 2;
+      constexpr int kCols = BN / kFixGroups;   // activation rows per group (>= 32)
+      const int fg = warp >> 2;
+      const bool mine =
+          fg < kFixGroups &&
+          PETIT_CHECK(f.d >= 0 && f.d < C::kNumD && f.c_first >= 0 && f.c_first <= cta &&
+                      cta <= f.c_last && f.c_last < P && f.first_slot >= 0 &&
+                      f.first_slot < 2 * NS);
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase +
                              f.d * BN + fg * kCols;
+      uint16_t* gst = reinterpret_cast<uint16_t*>(sm_a) + (fg % kFixGroups) * 16 * kTileN;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kCols; c0 += kLd) {
-        float own[kLd];
-#pragma unroll
-        for (int j = 0; j < kLd; ++j) own[j] = 0.0f;
-        bool have = false;
-#pragma unroll
-        for (int t = 0; t < C::kMmaThreads; ++t) {
-          if (f.has & (1u << t)) {
-            uint32_t x[kLd];
-            if constexpr (kLd == 16) {
-              tmem_ld_x16(tbase + (t * C::kNumD) * BN + c0, x);
-            } else {
-              tmem_ld_x4(tbase + (t * C::kNumD) * BN + c0, x);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < kLd; ++j) own[j] = have ? own[j] + __uint_as_float(x[j]) : __uint_as_float(x[j]);
-            have = true;
-          }
-        }
+      for (int c0 = 0; c0 < kCols; c0 += 16) {
         const int m0 = fg * kCols + c0;   // first activation row (tile-local)
-        float acc[kLd];
+        if (mine) {
+          float own[16];
+          bool have = false;
 #pragma unroll
-        for (int j = 0; j < kLd; ++j) acc[j] = 0.0f;
+          for (int t = 0; t < C::kMmaThreads; ++t) {
+            if (f.has & (1u << t)) {
+              uint32_t x[16];
+              tmem_ld_x16(tbase + (t * C::kNumD) * BN + c0, x);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                own[j] = have ? own[j] + __uint_as_float(x[j]) : __uint_as_float(x[j]);
+              have = true;
+            }
+          }
+          float acc[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll 1
-        for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
-          float tv[kFixBatch][kLd];
+          for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
+            float tv[kFixBatch][16];
 #pragma unroll
-          for (int x = 0; x < kFixBatch; ++x) {
-            const int64_t c = cb + x;
-            if (c <= f.c_last && c != cta) {
-              const float* src = p.partials +
-                                 static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * sid(c)) *
-                                     (BN * kTileN) +
-                                 m0 * kTileN + r;
+            for (int x = 0; x < kFixBatch; ++x) {
+              const int64_t c = cb + x;
+              if (c <= f.c_last && c != cta) {
+                const float* src =
+                    p.partials +
+                    static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * sid(c)) *
+                        (BN * kTileN) +
+                    m0 * kTileN + r;
 #pragma unroll
-              for (int j = 0; j < kLd; ++j) tv[x][j] = __ldcg(src + j * kTileN);
+                for (int j = 0; j < 16; ++j) tv[x][j] = __ldcg(src + j * kTileN);
+              }
+            }
+#pragma unroll
+            for (int x = 0; x < kFixBatch; ++x) {
+              const int64_t c = cb + x;
+              if (c <= f.c_last) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += c == cta ? own[j] : tv[x][j];
+              }
             }
           }
 #pragma unroll
-          for (int x = 0; x < kFixBatch; ++x) {
-            const int64_t c = cb + x;
-            if (c <= f.c_last) {
+          for (int j = 0; j < 16; ++j) gst[j * kTileN + r] = out_bits<FMT>(f.alpha * acc[j]);
+        }
+        __syncthreads();
+        if (mine) {
 #pragma unroll
-              for (int j = 0; j < kLd; ++j) acc[j] += c == cta ? own[j] : tv[x][j];
-            }
+          for (int s2 = 0; s2 < 2; ++s2) {
+            const int row = 4 * q + 2 * s2 + (lane >> 4);   // warp q writes rows 4q .. 4q + 3
+            const int col = (lane & 15) * 8;
+            const int64_t mrow = f.row0 + m0 + row;
+            if (mrow < f.g_rows &&
+                PETIT_CHECK(f.col0 + col + 8 <= p.n &&
+                            (f.c_g - p.c) + mrow * p.n + f.col0 + col + 8 <= p.chk_c_elems))
+              *reinterpret_cast<uint4*>(f.c_g + mrow * p.n + f.col0 + col) =
+                  *reinterpret_cast<const uint4*>(gst + row * kTileN + col);
           }
         }
-#pragma unroll
-        for (int j = 0; j < kLd; ++j) {
-          const int64_t mrow = f.row0 + m0 + j;
-          if (mrow < f.g_rows &&
-              PETIT_CHECK(f.col0 + r < p.n &&
-                          (f.c_g - p.c) + mrow * p.n + f.col0 + r < p.chk_c_elems))
-            f.c_g[mrow * p.n + f.col0 + r] = out_bits<FMT>(f.alpha * acc[j]);
+        __syncthreads();
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  } else {
+    if (fix->valid && !*abort_flag) {
+      const FixJob f = *fix;
+      constexpr int kFixGroups = C::kThreads / 32 >= 16 ? 4 : 2;
+      constexpr int kCols = BN / kFixGroups;               // activation rows per group
+      constexpr int kLd = kCols >= 16 ? 16 : 4;            // columns per tensor-memory load
+      const int fg = warp >> 2;
+      if (fg < kFixGroups && !*abort_flag &&
+          PETIT_CHECK(f.d >= 0 && f.d < C::kNumD && f.c_first >= 0 && f.c_first <= cta &&
+                      cta <= f.c_last && f.c_last < P && f.first_slot >= 0 &&
+                      f.first_slot < 2 * NS)) {
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::kDColBase +
+                               f.d * BN + fg * kCols;
+  #pragma unroll 1
+        for (int c0 = 0; c0 < kCols; c0 += kLd) {
+          float own[kLd];
+  #pragma unroll
+          for (int j = 0; j < kLd; ++j) own[j] = 0.0f;
+          bool have = false;
+  #pragma unroll
+          for (int t = 0; t < C::kMmaThreads; ++t) {
+            if (f.has & (1u << t)) {
+              uint32_t x[kLd];
+              if constexpr (kLd == 16) {
+                tmem_ld_x16(tbase + (t * C::kNumD) * BN + c0, x);
+              } else {
+                tmem_ld_x4(tbase + (t * C::kNumD) * BN + c0, x);
+              }
+              tmem_wait_ld();
+  #pragma unroll
+              for (int j = 0; j < kLd; ++j) own[j] = have ? own[j] + __uint_as_float(x[j]) : __uint_as_float(x[j]);
+              have = true;
+            }
+          }
+          const int m0 = fg * kCols + c0;   // first activation row (tile-local)
+          float acc[kLd];
+  #pragma unroll
+          for (int j = 0; j < kLd; ++j) acc[j] = 0.0f;
+  #pragma unroll 1
+          for (int64_t cb = f.c_first; cb <= f.c_last; cb += kFixBatch) {
+            float tv[kFixBatch][kLd];
+  #pragma unroll
+            for (int x = 0; x < kFixBatch; ++x) {
+              const int64_t c = cb + x;
+              if (c <= f.c_last && c != cta) {
+                const float* src = p.partials +
+                                   static_cast<size_t>(c == f.c_first ? f.first_slot : 2 * sid(c)) *
+                                       (BN * kTileN) +
+                                   m0 * kTileN + r;
+  #pragma unroll
+                for (int j = 0; j < kLd; ++j) tv[x][j] = __ldcg(src + j * kTileN);
+              }
+            }
+  #pragma unroll
+            for (int x = 0; x < kFixBatch; ++x) {
+              const int64_t c = cb + x;
+              if (c <= f.c_last) {
+  #pragma unroll
+                for (int j = 0; j < kLd; ++j) acc[j] += c == cta ? own[j] : tv[x][j];
+              }
+            }
+          }
+  #pragma unroll
+          for (int j = 0; j < kLd; ++j) {
+            const int64_t mrow = f.row0 + m0 + j;
+            if (mrow < f.g_rows &&
+                PETIT_CHECK(f.col0 + r < p.n &&
+                            (f.c_g - p.c) + mrow * p.n + f.col0 + r < p.chk_c_elems))
+              f.c_g[mrow * p.n + f.col0 + r] = out_bits<FMT>(f.alpha * acc[j]);
+          }
         }
       }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
   if constexpr (PAIR) {
     // Neither CTA of a pair frees its tensor memory or exits while the
