@@ -120,3 +120,30 @@ def test_pair_full_size_gate_up_prefill(cuda_lib):
     rows = np.concatenate([np.arange(0, 256), np.arange(n - 256, n), np.arange(300, n, 977)])
     codes, scales = oracle_quantize(w[rows].cpu(), "nvfp4", g)
     assert_parity(c[:, rows], oracle_reference(a.cpu(), codes, scales, "nvfp4", g), "gate_up m=256")
+
+
+@pytest.mark.parametrize("n,m", [(16384, 100), (57344, 200)])
+def test_full_tiles_write_no_row_past_m(cuda_lib, n, m):
+    """Whole 128/256-row output tiles are written through the shared-memory
+    stage in 256-byte row segments; with m not a multiple of the tile height
+    (n = 16384: one 128-row tile per CTA on 128 CTAs; n = 57344: CTA pairs,
+    256-row tiles) no row past m may be written, and sampled columns match
+    the oracle."""
+    k = 8192
+    w = synth.weights(n, k, seed=17, device="cuda")
+    g = cuda_lib.nvfp4_global_scale(cuda_lib.absmax(w).item())
+    wp, sp = cuda_lib.quantize(w, "nvfp4", g)
+    rep = cuda_lib.repack(wp, sp, "nvfp4")
+    torch.cuda.synchronize()
+    a = synth.activations(m, k, seed=18).cuda()
+    guard = 16
+    buf = torch.full((m + guard, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = cuda_lib.Workspace()
+    c = cuda_lib.gemm(a, rep, n, "nvfp4", g, workspace=ws, out=buf[:m])
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert torch.isnan(buf[m:].float()).all(), "a row past m was written"
+    assert not torch.isnan(c.float()).any()
+    rows = np.concatenate([np.arange(0, 128), np.arange(n - 128, n), np.arange(200, n, 1013)])
+    codes, scales = oracle_quantize(w[rows].cpu(), "nvfp4", g)
+    assert_parity(c[:, rows], oracle_reference(a.cpu(), codes, scales, "nvfp4", g), f"n={n} m={m}")
