@@ -7,14 +7,21 @@
 //
 // Design (one CTA per SM, persistent, stream-K):
 // * The MMA runs "swap-AB": 128 weight rows fill the tcgen05 M side, the m
-//   activation rows are the N side (16..128), so decode-sized m does not waste
+//   activation rows are the N side (16..256), so decode-sized m does not waste
 //   the tensor core (the pages' small-m, memory-bound regime: Petit blog,
 //   "Performance results").
 // * Work = (weight tile, activation tile, 128-k stage) units in tile-major
-//   order, split evenly over the CTAs; a CTA's range covers at most two
-//   partial tiles, whose FP32 partial sums go to the workspace.  The last CTA
-//   to finish a shared tile (atomic arrival counter, no waiting) adds the
-//   partials in a fixed order and writes C, so results are deterministic.
+//   order, split over the CTAs in contiguous ranges (stream-K); a CTA's range
+//   covers at most two partial tiles, whose FP32 partial sums go to the
+//   workspace.  The last CTA to finish a shared tile (atomic arrival counter,
+//   no waiting) adds the partials in a fixed order and writes C, so results
+//   are deterministic.
+// * CTA pairs (PAIR, for 128/256-row activation tiles): two CTAs of a
+//   cluster take adjacent 128-row weight tiles of one 256-row work tile and
+//   one thread of the even CTA issues cta_group::2 MMAs (M = 256); each CTA
+//   holds half of the activation rows.  The odd CTA's warp 1 forwards its
+//   activation-stage completions; its dequantisers and epilogue arrive on the
+//   even CTA's barriers; MMA completions are committed to both CTAs.
 // * A pipeline unit is KU (1 or 2) consecutive 128-k chunks of one tile.
 //   Its data arrives with exactly two copies: one bulk copy of the repacked
 //   codes + scales (contiguous) and one 3-D TMA box holding all 2*KU 64-k
@@ -23,8 +30,11 @@
 // * Warp roles:
 //     warp 0      producer: the two copies per unit into a ring of
 //                 shared-memory stages (mbarrier full/empty);
-//     warp 1      tensor-memory owner and MMA issuer (one elected lane);
-//     warps 2-5   epilogue: tensor memory -> registers -> C or partials;
+//     warps 1, 14, 15  tensor-memory owner (warp 1) and MMA issuers (one
+//                 elected lane each; one issuer at N = 64, 256 and in pairs);
+//     warps 2-5   epilogue: tensor memory -> registers -> C or partials
+//                 (128/256-row tiles: C through a 16-row shared-memory stage,
+//                 in whole 256-byte row segments);
 //     warps 6-13  dequantisers: shared memory -> registers -> BF16 -> tensor
 //                 memory, where the MMA reads its A operand.  Each thread owns
 //                 one weight row (= one tensor-memory lane).
