@@ -657,6 +657,12 @@ def run_ours(args, rank, world, local):
 
     sampler.stop()
     clocks = sampler.summary(windows)
+    # every GEMM of this run used `ws`: a bounded device wait that ran out
+    # (or, in the bounds-checking build, a failed index check) would show here
+    device_status = ws.status()
+    if device_status != 0:
+        raise RuntimeError(f"device status {binding.STATUS.get(device_status, device_status)} "
+                           "after the benchmark: its numbers are not valid")
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -689,6 +695,7 @@ def run_ours(args, rank, world, local):
             "prefill_m256": prefill, "mxfp4_decode": mxfp4, "fp16_decode_m16": fp16_decode,
             "m_sweep": m_sweep,
             "moe_mxfp4_gate_up": moe, "cublas_bf16_context": cublas,
+            "device_status": binding.STATUS.get(device_status, device_status),
         }
         print(json.dumps(out), flush=True)
 
