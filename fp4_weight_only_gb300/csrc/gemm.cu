@@ -501,6 +501,24 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
     if (!*abort_flag) fail();
     return false;
   };
+  // Waits in code that all 32 lanes of a warp run together, with warp
+  // barriers and warp-collective tensor-memory stores after them, must give
+  // every lane the same answer.  try_wait may suspend each lane on its own,
+  // so a lane that checked the CTA's abort flag just as the phase completed
+  // could leave the loop while the others go on, and they would then wait at
+  // the next warp barrier without a time limit.  The dequantisers and the
+  // epilogue therefore wait on the phase and the 2 s limit only (after an
+  // abort elsewhere their phases stop completing, and every lane runs out
+  // together); the MMA issuers and the activation forwarder, whose waits
+  // cost little, vote instead and stop at once.
+  auto wait_lane = [&](uint64_t* bar, uint32_t parity) {
+    if (mbar_wait_bounded(smem_u32(bar), parity, p.timeout_ns, nullptr)) return true;
+    if (!*abort_flag) fail();
+    return false;
+  };
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait(bar, parity));
+  };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -613,7 +631,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
     uint32_t ph = 0;
     for (int32_t i = 0; i < nu; ++i) {
       if (!PETIT_CHECK(st >= 0 && st < C::kXStages)) break;
-      if (!__all_sync(0xffffffffu, wait(&xfull[st], ph))) break;
+      if (!wait_warp(&xfull[st], ph)) break;
       if (elect_one()) mbar_arrive_remote(mapa_shared(smem_u32(&xpeer[st]), 0));
       __syncwarp();
       if (++st == C::kXStages) {
@@ -631,9 +649,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
     // issues the MMAs and commits.  (Issued from a lone lane-0 branch each
     // MMA cost ~65 cycles of issue, which set the pace of the MMA chain.)
     {
-      auto uwait = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, wait(bar, parity));
-      };
+      auto uwait = [&](uint64_t* bar, uint32_t parity) { return wait_warp(bar, parity); };
 
       // Segments (the CTA's units inside one tile) in order; inside a
       // segment only this issuer's units i = t, t + kMmaThreads, ...
@@ -777,7 +793,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
     auto epi_sync = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(epi_bar));
-      const bool ok = wait(epi_bar, epi_phase & 1u);
+      const bool ok = wait_lane(epi_bar, epi_phase & 1u);
       ++epi_phase;
       return ok;
     };
@@ -840,7 +856,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
           *epi_flag = ld_acquire_gpu(ctr) == static_cast<uint32_t>(c_last - c_first);
       }
       if (!PETIT_CHECK(d >= 0 && d < C::kNumD)) break;
-      if (!wait(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
+      if (!wait_lane(&dfull[d], static_cast<uint32_t>((seg / C::kNumD) & 1))) break;
       tc_fence_after();
       // issuer t wrote its accumulator iff the segment holds a unit with
       // CTA-local index i % kMmaThreads == t
@@ -1036,7 +1052,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
       if (!PETIT_CHECK(st >= 0 && st < C::kWStages && b >= 0 && b < C::kNumA && st2 >= 0 &&
                        st2 < C::kXStages))
         break;
-      if (!wait(&wfull[st], ph)) break;
+      if (!wait_lane(&wfull[st], ph)) break;
       bool ok = true;
       if constexpr (FMT == kMXFP4) {
         // The repack's per-chunk flag bytes (warp-uniform), read once per
@@ -1072,7 +1088,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
             if (hj == 0 && i >= C::kNumA) {
               // A-buffer b was last used by unit i - kNumA: wait for its
               // MMAs, and order the stores below after their operand reads
-              if (!wait(&mdone[st2], ph2)) {
+              if (!wait_lane(&mdone[st2], ph2)) {
                 ok = false;
                 break;
               }
@@ -1107,7 +1123,7 @@ __global__ void __launch_bounds__((Cfg<FMT, BN, KU, PAIR>::kThreads), 1)
           if (hj == 0 && i >= C::kNumA) {
             // A-buffer b was last used by unit i - kNumA: wait for its MMAs,
             // and order the stores below after their operand reads
-            if (!wait(&mdone[st2], ph2)) {
+            if (!wait_lane(&mdone[st2], ph2)) {
               ok = false;
               break;
             }

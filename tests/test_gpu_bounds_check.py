@@ -147,8 +147,12 @@ def _limited(chk, weight_bytes, c_elems, fn):
         assert L.petit_check_set_limits(-1, -1) == 0
 
 
-def test_failed_weight_check_reports_bounds_and_recovers(chk):
-    n, k, m = 1024, 8192, 16          # split tiles: arrival counters in use
+@pytest.mark.parametrize("m", [16, 200])
+def test_failed_weight_check_reports_bounds_and_recovers(chk, m):
+    """m = 16: single CTAs; m = 200: CTA pairs (256-row tiles), where the CTA
+    that stops leaves its partner to run out its bounded waits and both
+    meet at the final cluster barrier."""
+    n, k = 1024, 8192                 # split tiles: arrival counters in use
     w = synth.weights(n, k, seed=81)
     codes, scales, rep = _prep(chk, w, "nvfp4")
     a = synth.activations(m, k, seed=82).cuda()
