@@ -40,6 +40,15 @@ _c_i64 = ctypes.c_int64
 _c_p = ctypes.c_void_p
 _c_sz = ctypes.c_size_t
 
+
+class PlanInfo(ctypes.Structure):
+    """petit_plan_info_t"""
+    _fields_ = [("bn", ctypes.c_int32), ("ku", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
+                ("num_ranges", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("units_per_tile", ctypes.c_int32), ("num_tiles", ctypes.c_int64),
+                ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "petit_layout_version": (ctypes.c_int, []),
@@ -76,6 +85,11 @@ SIGNATURES = {
     "petit_bounds_checking": (ctypes.c_int, []),
     "petit_check_set_limits": (ctypes.c_int, [_c_i64, _c_i64]),
     "petit_selftest_timeout": (ctypes.c_int, [_c_p, _c_sz, ctypes.c_uint32, _c_p]),
+    "petit_plan_gemm": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(PlanInfo), _c_p, _c_i64]),
+    "petit_plan_moe": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_i64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.POINTER(PlanInfo), _c_p, _c_i64]),
+    "petit_device_limits": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -318,6 +332,56 @@ def set_pair_mode(mode=0):
     apply."""
     _check(load().petit_set_pair_mode(int(mode)), "set_pair_mode")
     workspace_bytes.cache_clear()
+
+
+_MAX_RANGES = 1025   # kernel grids have at most 1024 work ranges
+
+
+def _plan_result(info, starts):
+    d = {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+    d["cta_pairs"] = bool(d["cta_pairs"])
+    d["range_starts"] = list(starts[:info.num_ranges + 1]) if info.num_ranges else []
+    return d
+
+
+def plan(m, n, k, fmt="nvfp4", num_sms=None, pair_capacity=None):
+    """The plan of a GEMM (tile shape, CTA pairs, work units and ranges,
+    workspace bytes) on a device with num_sms SMs and pair_capacity resident
+    CTA pairs; by default the current device's (petit_device_limits).  With
+    both given, no GPU is needed."""
+    L = load()
+    if num_sms is None or pair_capacity is None:
+        dev_sms, dev_pc = device_limits()
+        num_sms = dev_sms if num_sms is None else num_sms
+        pair_capacity = dev_pc if pair_capacity is None else pair_capacity
+    info = PlanInfo()
+    starts = (ctypes.c_int64 * _MAX_RANGES)()
+    _check(L.petit_plan_gemm(int(m), int(n), int(k), FORMATS[fmt], int(num_sms), int(pair_capacity),
+                             ctypes.byref(info), starts, _MAX_RANGES), "plan_gemm")
+    return _plan_result(info, starts)
+
+
+def moe_plan(expert_offsets, n, k, fmt="mxfp4", num_sms=None, pair_capacity=None):
+    """:func:`plan` for the grouped MoE GEMM (expert_offsets: E + 1 row offsets)."""
+    L = load()
+    if num_sms is None or pair_capacity is None:
+        dev_sms, dev_pc = device_limits()
+        num_sms = dev_sms if num_sms is None else num_sms
+        pair_capacity = dev_pc if pair_capacity is None else pair_capacity
+    E = len(expert_offsets) - 1
+    off = (ctypes.c_int64 * (E + 1))(*[int(x) for x in expert_offsets])
+    info = PlanInfo()
+    starts = (ctypes.c_int64 * _MAX_RANGES)()
+    _check(L.petit_plan_moe(off, E, int(n), int(k), FORMATS[fmt], int(num_sms), int(pair_capacity),
+                            ctypes.byref(info), starts, _MAX_RANGES), "plan_moe")
+    return _plan_result(info, starts)
+
+
+def device_limits():
+    """(SM count, resident CTA pairs) of the current device, as the GEMMs plan with."""
+    sms, pc = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().petit_device_limits(ctypes.byref(sms), ctypes.byref(pc)), "device_limits")
+    return sms.value, pc.value
 
 
 def selftest_timeout(workspace, timeout_us=1000):

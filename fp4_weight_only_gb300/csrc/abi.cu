@@ -233,6 +233,39 @@ petit_status_t moe_common(int fmt, const void* A, const uint8_t* rep, const floa
   return from_cuda(petit::launch_gemm(plan, args, map, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Arguments of the plan queries that do not depend on the problem.
+petit_status_t check_plan_args(int num_sms, int pair_cap, const petit_plan_info_t* info) {
+  if (!info || num_sms < 1 || num_sms > petit::kMaxCtas || pair_cap < 0 ||
+      pair_cap > petit::kMaxBoundCtas)
+    return PETIT_ERR_INVALID_ARG;
+  return PETIT_OK;
+}
+
+// A plan as the public struct, and its ranges: the first unit of range c is
+// the kernel's own cta_lo(c) (explicit bounds, else the even split
+// c * (U / P) + c * (U % P) / P).
+petit_status_t describe_plan(const petit::GemmPlan& pl, petit_plan_info_t* info,
+                             int64_t* starts, int64_t max_ranges) {
+  if (pl.units >= kMaxUnits) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  std::memset(info, 0, sizeof(*info));
+  info->bn = pl.bn;
+  info->ku = pl.ku;
+  info->cta_pairs = pl.pair ? 1 : 0;
+  info->num_ranges = pl.num_ctas;
+  info->num_ctas = pl.num_ctas * (pl.pair ? 2 : 1);
+  info->units_per_tile = pl.k_stages / pl.ku;
+  info->num_tiles = info->units_per_tile > 0 ? pl.units / info->units_per_tile : 0;
+  info->units = pl.units;
+  info->workspace_bytes = pl.ws.total;
+  if (!starts) return PETIT_OK;
+  const int64_t P = pl.num_ctas;
+  if (max_ranges < P + 1) return PETIT_ERR_INVALID_ARG;
+  const int64_t q = pl.units / P, r = pl.units % P;
+  for (int64_t c = 0; c <= P; ++c)
+    starts[c] = c == P ? pl.units : pl.use_bounds ? pl.bound[c] : c * q + (c * r) / P;
+  return PETIT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -424,6 +457,45 @@ petit_status_t petit_set_tile_config(int bn, int ku) {
 
 petit_status_t petit_set_pair_mode(int mode) {
   return petit::set_pair_mode(mode) ? PETIT_OK : PETIT_ERR_INVALID_ARG;
+}
+
+petit_status_t petit_plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms,
+                               int pair_capacity, petit_plan_info_t* info,
+                               int64_t* range_starts, int64_t max_ranges) {
+  if (petit_status_t st = check_plan_args(num_sms, pair_capacity, info)) return st;
+  if (m < 1) return PETIT_ERR_INVALID_ARG;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4 && fmt != PETIT_FMT_NVFP4_F16)
+    return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (m > kMaxDim) return PETIT_ERR_UNSUPPORTED_SHAPE;
+  return describe_plan(petit::plan_gemm(m, n, k, fmt, num_sms, pair_capacity), info,
+                       range_starts, max_ranges);
+}
+
+petit_status_t petit_plan_moe(const int64_t* expert_offsets, int64_t num_experts, int64_t n,
+                              int64_t k, int fmt, int num_sms, int pair_capacity,
+                              petit_plan_info_t* info, int64_t* range_starts,
+                              int64_t max_ranges) {
+  if (petit_status_t st = check_plan_args(num_sms, pair_capacity, info)) return st;
+  if (fmt != PETIT_FMT_NVFP4 && fmt != PETIT_FMT_MXFP4) return PETIT_ERR_INVALID_ARG;
+  if (petit_status_t st = check_offsets(expert_offsets, num_experts)) return st;
+  if (petit_status_t st = check_tiled_shape(n, k)) return st;
+  if (expert_offsets[num_experts] == 0) {   // the GEMM launches nothing
+    std::memset(info, 0, sizeof(*info));
+    return PETIT_OK;
+  }
+  return describe_plan(petit::plan_grouped(expert_offsets, static_cast<int>(num_experts), n, k,
+                                           fmt, num_sms, pair_capacity),
+                       info, range_starts, max_ranges);
+}
+
+petit_status_t petit_device_limits(int* num_sms, int* pair_capacity) {
+  if (!num_sms || !pair_capacity) return PETIT_ERR_INVALID_ARG;
+  int sms = 0, pc = 0;
+  if (petit_status_t st = current_device(&sms, nullptr, &pc)) return st;
+  *num_sms = sms;
+  *pair_capacity = pc;
+  return PETIT_OK;
 }
 
 int petit_bounds_checking(void) { return petit::bounds_checking() ? 1 : 0; }

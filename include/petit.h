@@ -319,6 +319,59 @@ petit_status_t petit_set_tile_config(int bn, int ku);
  * PETIT_ERR_INVALID_ARG for any other mode. */
 petit_status_t petit_set_pair_mode(int mode);
 
+/* The plan a GEMM would run with, for tile tuning and for checking the
+ * planner without a GPU (Petit PyPI page, "Known limitations": tile
+ * parameters may need tuning for a given matrix size).  One launch runs a
+ * persistent grid: the output is cut into work tiles of bn activation rows
+ * by 128 weight rows (256 with CTA pairs), a tile along k into
+ * units_per_tile work units of ku 128-k chunks, and the units, numbered
+ * tile by tile with k fastest, into num_ranges consecutive ranges ("stream-K"
+ * split: a tile whose units fall into several ranges is summed from their
+ * FP32 partials in the workspace). */
+typedef struct petit_plan_info {
+  int32_t bn;              /* activation rows per tile (the MMA N side) */
+  int32_t ku;              /* 128-k chunks per work unit (1 or 2) */
+  int32_t cta_pairs;       /* 1: clusters of two CTAs issuing M = 256 MMAs */
+  int32_t num_ranges;      /* work ranges: one per CTA, or per CTA pair */
+  int32_t num_ctas;        /* CTAs launched (twice num_ranges with CTA pairs) */
+  int32_t units_per_tile;  /* work units along k of one tile */
+  int64_t num_tiles;       /* work tiles, over all activation tiles and groups */
+  int64_t units;           /* num_tiles * units_per_tile */
+  uint64_t workspace_bytes; /* workspace the GEMM needs on such a device */
+} petit_plan_info_t;
+
+/* Plans C[m, n] = A . Wq^T (arguments as for the GEMM entry points; fmt a
+ * petit_format_t) for a device with `num_sms` SMs (1..1024) that holds
+ * `pair_capacity` CTA pairs of the pair kernels at once (0..160; 0 plans
+ * without CTA pairs), under this process's current petit_set_tile_config and
+ * petit_set_pair_mode settings.  No device is touched; on the current
+ * device the GEMM runs exactly this plan when num_sms and pair_capacity are
+ * petit_device_limits()'s values.  *info receives the plan.  range_starts:
+ * NULL, or a host array of max_ranges entries that receives the first unit
+ * of every range and then `units` (num_ranges + 1 values, non-decreasing,
+ * every range non-empty); when max_ranges is smaller than that, *info is
+ * still written and PETIT_ERR_INVALID_ARG is returned.
+ * Errors: INVALID_ARG (null info, m < 1, a bad format, num_sms or
+ * pair_capacity out of range, range_starts too short), UNSUPPORTED_SHAPE (as
+ * for the GEMM). */
+petit_status_t petit_plan_gemm(int64_t m, int64_t n, int64_t k, int fmt, int num_sms,
+                               int pair_capacity, petit_plan_info_t* info,
+                               int64_t* range_starts, int64_t max_ranges);
+
+/* The same for the grouped MoE GEMM (expert_offsets and num_experts as for
+ * petit_moe_gemm_bf16_mxfp4; fmt PETIT_FMT_MXFP4 or PETIT_FMT_NVFP4).  No
+ * routed tokens (expert_offsets[num_experts] = 0) plans nothing: *info is
+ * zeroed and PETIT_OK returned. */
+petit_status_t petit_plan_moe(const int64_t* expert_offsets, int64_t num_experts, int64_t n,
+                              int64_t k, int fmt, int num_sms, int pair_capacity,
+                              petit_plan_info_t* info, int64_t* range_starts,
+                              int64_t max_ranges);
+
+/* The current device's SM count and how many CTA pairs of the pair kernels
+ * it holds at once (the values the GEMM entry points plan with).  Errors:
+ * INVALID_ARG (a null pointer), CUDA (no usable device), ARCH (not sm_103). */
+petit_status_t petit_device_limits(int* num_sms, int* pair_capacity);
+
 /* ------------------------------------------------- bounds-checking build */
 
 /* The library also builds as _petit_check.so with every global-memory
