@@ -225,7 +225,10 @@ def l2_bytes(dev):
 def oracle_sample(weights_cpu, acts_cpu, rows, min_seconds=0.0):
     """Time the FP64 oracle (dequant + GEMM) on the first `rows` rows of each
     weight matrix; quantisation is done first and not timed.  The timed pass
-    over the four matrices repeats until `min_seconds` have elapsed."""
+    over the four matrices repeats until `min_seconds` have elapsed.
+    Returns (bytes, wall s, passes, process CPU s): the CPU time of all the
+    process's threads over the wall time is how many cores the oracle kept
+    busy (numpy's dequantise runs on one, its BLAS matrix product on a pool)."""
     from oracle import gemm as og
     from oracle import quantize as oq
     prepared = []
@@ -234,6 +237,7 @@ def oracle_sample(weights_cpu, acts_cpu, rows, min_seconds=0.0):
         prepared.append((a.float().numpy(), codes, scales, k))
     per_pass = sum(algo_bytes(M_DECODE, rows, k) for _, _, _, k in prepared)
     passes = 0
+    c0 = time.process_time()
     t0 = time.perf_counter()
     while True:
         for a, codes, scales, k in prepared:
@@ -242,7 +246,12 @@ def oracle_sample(weights_cpu, acts_cpu, rows, min_seconds=0.0):
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
             break
-    return per_pass * passes, dt, passes
+    return per_pass * passes, dt, passes, time.process_time() - c0
+
+
+def busy_cores(cpu_s, wall_s):
+    """Cores kept busy on average (at least 1), from process CPU and wall time."""
+    return max(1, round(cpu_s / wall_s)) if wall_s > 0 else 1
 
 
 def synth_inputs_cpu(rows):
@@ -266,15 +275,17 @@ def run_reference(args, rank, world):
     ws, acts = synth_inputs_cpu(rows)
     for _ in range(max(args.warmup, 0)):
         oracle_sample(ws, acts, rows)
-    total_b, total_t = 0, 0.0
+    total_b, total_t, total_c = 0, 0.0, 0.0
     for _ in range(args.steps):
-        b, t, _ = oracle_sample(ws, acts, rows)
+        b, t, _, c = oracle_sample(ws, acts, rows)
         total_b += b
         total_t += t
+        total_c += c
     value = total_b / total_t / 1e9
+    cores = busy_cores(total_c, total_t)
     sample = (f"{rows} seeded N(0,0.02) rows for each of the 4 Llama-3-70B weight shapes, m={M_DECODE}; "
-              "oracle NVFP4 dequantise + FP64 GEMM per step (quantisation untimed)")
-    cores = os.cpu_count()
+              "oracle NVFP4 dequantise + FP64 GEMM per step (quantisation untimed); "
+              f"{total_c:.1f} s of CPU in {total_t:.1f} s on a {os.cpu_count()}-core host")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
@@ -669,12 +680,13 @@ def run_ours(args, rank, world, local):
         rows = 512
         w_cpu = [synth.weights(n, k, seed=100 + i, device=dev)[:rows].cpu() for i, (_, n, k) in enumerate(SHAPES)]
         a_cpu = [a.cpu() for a in acts]
-        nb, dt, passes = oracle_sample(w_cpu, a_cpu, rows, min_seconds=10.0)
-        cpu_baseline = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+        nb, dt, passes, cpu_s = oracle_sample(w_cpu, a_cpu, rows, min_seconds=10.0)
+        cpu_baseline = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": busy_cores(cpu_s, dt),
                         "kind": "oracle",
                         "sample": f"first {rows} rows of each of the 4 weight matrices (same seeded weights), "
                                   f"m={M_DECODE}; NVFP4 dequantise + FP64 GEMM with numpy (BLAS threads), "
-                                  f"quantisation untimed; {passes} passes in {dt:.1f} s"}
+                                  f"quantisation untimed; {passes} passes in {dt:.1f} s using {cpu_s:.1f} s "
+                                  f"of CPU on a {os.cpu_count()}-core host (cores = CPU / wall time)"}
 
     if rank == 0:
         out = {
