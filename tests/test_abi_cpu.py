@@ -125,3 +125,24 @@ def test_bounds_checking_build_loads_and_differs_only_in_checks(lib):
     assert chk.petit_check_set_limits(-1, -1) == 0
     assert chk.petit_layout_version() == lib.petit_layout_version()
     assert chk.petit_repacked_bytes(4096, 4096, 1) == lib.petit_repacked_bytes(4096, 4096, 1)
+
+
+def test_binding_has_no_cpu_fallback(lib):
+    """The Python entry points refuse host tensors instead of computing on
+    the CPU, and with no GPU the device queries fail with a status."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a = torch.zeros(16, 1024, dtype=torch.bfloat16)
+    rep = torch.zeros(binding.load().petit_repacked_bytes(1024, 1024, 0), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.gemm(a, rep, 1024, "nvfp4")
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.quantize(torch.zeros(128, 128, dtype=torch.bfloat16), "nvfp4")
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.FP4Weight(torch.zeros(128, 128, dtype=torch.bfloat16), "mxfp4")
+    with pytest.raises(binding.PetitError) as e:
+        binding.device_limits()
+    assert e.value.status == 6
+    # the plan itself needs no device
+    assert binding.plan(16, 1024, 1024, "nvfp4", num_sms=152, pair_capacity=76)["bn"] == 16
