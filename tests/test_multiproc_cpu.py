@@ -45,7 +45,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_slowest_time():
     world, port = 2, _free_port()
-    with mp.Manager() as manager:
+    with mp.get_context("spawn").Manager() as manager:
         out = manager.dict()
         mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True,
                            start_method="spawn")
