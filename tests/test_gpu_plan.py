@@ -65,3 +65,15 @@ def test_gemm_runs_in_exactly_the_planned_workspace(cuda_lib, m, pair_mode):
     finally:
         cuda_lib.set_pair_mode(0)
     assert_parity(out, oracle_reference(a.cpu(), codes, scales, "mxfp4"), f"m={m} pairs={pair_mode}")
+
+
+def test_tuner_times_every_tile_shape(cuda_lib):
+    from fp4_weight_only_gb300 import tune
+    m, n, k = 40, 1024, 1024
+    rows, planned, planned_us = tune.tune(m, n, k, "nvfp4", iters=8)
+    want = {(bn, ku, mode) for bn, ku in tune.candidates(k)
+            for mode in ((1, 2) if bn >= 128 else (1,))}
+    assert {(r["bn"], r["ku"], r["pair_mode"]) for r in rows} == want
+    assert all(r["us"] > 0 for r in rows) and planned_us > 0
+    assert [r["us"] for r in rows] == sorted(r["us"] for r in rows)
+    assert planned == cuda_lib.plan(m, n, k, "nvfp4")   # settings restored

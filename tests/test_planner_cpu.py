@@ -221,3 +221,17 @@ def test_plan_errors():
     assert L.petit_plan_moe(off, 2, 1024, 1024, 1, SMS, PAIRS, binding.ctypes.byref(info), None, 0) == INVALID
     off = (binding.ctypes.c_int64 * 3)(0, 5, 9)
     assert L.petit_plan_moe(off, 2, 1024, 1024, 2, SMS, PAIRS, binding.ctypes.byref(info), None, 0) == INVALID
+
+
+def test_tune_plan_only_cli(capsys):
+    from fp4_weight_only_gb300 import tune
+    assert tune.main(["--m", "128", "--n", "8192", "--k", "8192", "--plan-only",
+                      "--sms", str(SMS), "--pairs", str(PAIRS), "--json"]) == 0
+    import json
+    assert json.loads(capsys.readouterr().out) == binding.plan(128, 8192, 8192, "nvfp4", SMS, PAIRS)
+    assert tune.main(["--m", "16", "--n", "1024", "--k", "1024", "--fmt", "mxfp4", "--plan-only",
+                      "--sms", str(SMS), "--pairs", str(PAIRS)]) == 0
+    assert capsys.readouterr().out.startswith("bn=16 ku=2 single ranges=32")
+    # two 128-k chunks per unit only where k holds an even number of them
+    assert (16, 2) in tune.candidates(1024) and (16, 2) not in tune.candidates(384)
+    assert all(ku == 1 for _, ku in tune.candidates(1152))
