@@ -337,6 +337,15 @@ def set_pair_mode(mode=0):
 _MAX_RANGES = 1025   # kernel grids have at most 1024 work ranges
 
 
+def _limits(num_sms, pair_capacity):
+    """The given SM count and pair capacity, the current device's for any left out."""
+    if num_sms is None or pair_capacity is None:
+        dev_sms, dev_pc = device_limits()
+        num_sms = dev_sms if num_sms is None else num_sms
+        pair_capacity = dev_pc if pair_capacity is None else pair_capacity
+    return int(num_sms), int(pair_capacity)
+
+
 def _plan_result(info, starts):
     d = {f: getattr(info, f) for f, _ in PlanInfo._fields_}
     d["cta_pairs"] = bool(d["cta_pairs"])
@@ -350,13 +359,10 @@ def plan(m, n, k, fmt="nvfp4", num_sms=None, pair_capacity=None):
     CTA pairs; by default the current device's (petit_device_limits).  With
     both given, no GPU is needed."""
     L = load()
-    if num_sms is None or pair_capacity is None:
-        dev_sms, dev_pc = device_limits()
-        num_sms = dev_sms if num_sms is None else num_sms
-        pair_capacity = dev_pc if pair_capacity is None else pair_capacity
+    num_sms, pair_capacity = _limits(num_sms, pair_capacity)
     info = PlanInfo()
     starts = (ctypes.c_int64 * _MAX_RANGES)()
-    _check(L.petit_plan_gemm(int(m), int(n), int(k), FORMATS[fmt], int(num_sms), int(pair_capacity),
+    _check(L.petit_plan_gemm(int(m), int(n), int(k), FORMATS[fmt], num_sms, pair_capacity,
                              ctypes.byref(info), starts, _MAX_RANGES), "plan_gemm")
     return _plan_result(info, starts)
 
@@ -364,15 +370,12 @@ def plan(m, n, k, fmt="nvfp4", num_sms=None, pair_capacity=None):
 def moe_plan(expert_offsets, n, k, fmt="mxfp4", num_sms=None, pair_capacity=None):
     """:func:`plan` for the grouped MoE GEMM (expert_offsets: E + 1 row offsets)."""
     L = load()
-    if num_sms is None or pair_capacity is None:
-        dev_sms, dev_pc = device_limits()
-        num_sms = dev_sms if num_sms is None else num_sms
-        pair_capacity = dev_pc if pair_capacity is None else pair_capacity
+    num_sms, pair_capacity = _limits(num_sms, pair_capacity)
     E = len(expert_offsets) - 1
     off = (ctypes.c_int64 * (E + 1))(*[int(x) for x in expert_offsets])
     info = PlanInfo()
     starts = (ctypes.c_int64 * _MAX_RANGES)()
-    _check(L.petit_plan_moe(off, E, int(n), int(k), FORMATS[fmt], int(num_sms), int(pair_capacity),
+    _check(L.petit_plan_moe(off, E, int(n), int(k), FORMATS[fmt], num_sms, pair_capacity,
                             ctypes.byref(info), starts, _MAX_RANGES), "plan_moe")
     return _plan_result(info, starts)
 
